@@ -1,0 +1,374 @@
+#!/usr/bin/env python3
+"""Benchmark of the StreamBP language-model head on GB300 (one JSON line on stdout).
+
+Workload: SFT cross-entropy forward + backward of the LM head through the C ABI
+(``sbp_lmhead_sft``), bf16 operands with fp32 accumulation, T = 16384 tokens
+(8 x 2048), d = 4096, V = 151936, chunk = 2048; H ~ N(0,1), W ~ N(0, 0.02^2),
+labels uniform with 10% ignored -- synthetic, Qwen3-shaped.  One step = one call =
+the whole hot path (label scan, 8 x [forward GEMM + statistics, combine, logit
+gradient, dH/dW GEMMs, dH reduce], loss reduction) over one batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU; every rank processes its own batch
+(weak scaling, no collective on the data path); the timing is the max over ranks.
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T16384_d4096_V151936_chunk2048", objective="sft", T=16384, d=4096,
+                V=151936, chunk=2048, dtype="bf16", seed=1002, mask="frac", frac=0.1)
+METRIC = "lm_head fwd+bwd tokens/s (SFT CE, d=4096, V=151936) and % BF16 tensor peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CPU_SAMPLE_TOKENS = 384
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {}
+            for k in FALLBACK_PEAKS:
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[k] = float(v)
+            if "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                out.setdefault("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id is not None:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_id_for(torch, dev) -> str | None:
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ------------------------------------------------------------------------------- distributed
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def aggregate(torch, dist, tokens_local: float, ms_local: float, device) -> tuple[float, float]:
+    """Whole-job tokens (sum over ranks) and the step time (max over ranks)."""
+    if dist is None or not dist.is_initialized():
+        return tokens_local, ms_local
+    t = torch.tensor([tokens_local], dtype=torch.float64, device=device)
+    m = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(t.item()), float(m.item())
+
+
+# ------------------------------------------------------------------------------------ inputs
+
+def make_inputs(rank: int, T: int | None = None):
+    from memory_efficient_exact_gb300 import inputs as I
+    w = WORKLOAD
+    T = w["T"] if T is None else T
+    H, W = I.make_hw(T, w["d"], w["V"], w["seed"] + rank, w["dtype"])
+    y = I.make_labels(T, w["V"], w["seed"] + rank, w["mask"], w["frac"])
+    return H, W, y
+
+
+def cpu_oracle_sample(H, W, y, tokens: int):
+    """Times the float64 oracle (as it stands) on the first `tokens` tokens."""
+    from oracle import lmhead as O
+    t0 = time.perf_counter()
+    O.sft(H[:tokens], W, y[:tokens])
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------------- reference
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOAD
+    H, W, y = make_inputs(0, T=CPU_SAMPLE_TOKENS)
+    cpu_oracle_sample(H, W, y, 16)  # warm-up: BLAS threads, page-in
+    times = [cpu_oracle_sample(H, W, y, CPU_SAMPLE_TOKENS) for _ in range(args.steps)]
+    sec = sum(times)
+    value = CPU_SAMPLE_TOKENS * args.steps / sec
+    sample = (f"first {CPU_SAMPLE_TOKENS} tokens of the workload per step (full V and d), "
+              "numpy float64 with BLAS on all host cores")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {k: w[k] for k in ("workload", "T", "d", "V", "chunk")},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    rank, world, local_rank = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from memory_efficient_exact_gb300 import _build
+    _build.build_library()
+    from memory_efficient_exact_gb300 import sbp
+
+    w = WORKLOAD
+    T, d, V, chunk = w["T"], w["d"], w["V"], w["chunk"]
+    H, W, y = make_inputs(rank)
+    Ht = torch.from_numpy(H).to(dev).to(torch.bfloat16)
+    Wt = torch.from_numpy(W).to(dev).to(torch.bfloat16)
+    yt = torch.from_numpy(y).to(dev)
+    ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT, dev)
+    dH = torch.empty_like(Ht)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    st = torch.zeros((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return sbp.sft(Ht, Wt, yt, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        out = step()
+    torch.cuda.synchronize(dev)
+    sbp.check_status(st, "warm-up")
+    launches_per_call = sbp.last_launch_count()
+
+    # ---- device-timed region: inputs resident in HBM (larger than L2: W is 1.24 GB) ----
+    clocks = ClockSampler(gpu_id_for(torch, dev))
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sbp.profile_read()
+    sbp.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        out = step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sbp.profile_enable(False)
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    prof = sbp.profile_read()
+    sbp.check_status(st, "timed region")
+    ms_local = e0.elapsed_time(e1)
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    loss = float(out["loss"].item())
+
+    tokens_all, ms = aggregate(torch, dist, float(T * args.steps), ms_local, dev)
+    value = tokens_all / (ms / 1000.0)
+    ms_per_step = ms / args.steps
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside ----
+    Hh = torch.from_numpy(H).to(torch.bfloat16).pin_memory()
+    yh = torch.from_numpy(y).pin_memory()
+    dHh = torch.empty(Hh.shape, dtype=torch.bfloat16).pin_memory()
+    lossh = torch.empty((), dtype=torch.float32).pin_memory()
+    Hd = torch.empty_like(Ht)
+    yd = torch.empty_like(yt)
+
+    def e2e_step():
+        Hd.copy_(Hh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        o = sbp.sft(Hd, Wt, yd, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
+        dHh.copy_(o["dH"], non_blocking=True)
+        lossh.copy_(o["loss"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize(dev)
+    sbp.check_status(st, "e2e region")
+    e2e_tokens, e2e_ms = aggregate(torch, dist, float(T * args.steps), e2.elapsed_time(e3), dev)
+    h2d = Hh.numel() * Hh.element_size() + yh.numel() * yh.element_size()
+    d2h = dHh.numel() * dHh.element_size() + lossh.element_size()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    n_chunks = (T + chunk - 1) // chunk
+    bwd_ms, bwd_n = prof["backward_gemm"]
+    fwd_ms, fwd_n = prof["forward_gemm"]
+    grad_ms, grad_n = prof["logit_grad"]
+    oth_ms, oth_n = prof["other"]
+    flops_bwd_launch = 4.0 * chunk * d * V          # dH and dW GEMMs of one chunk (algorithmic)
+    flops_fwd_launch = 2.0 * chunk * d * V
+    bwd_avg_s = bwd_ms / max(bwd_n, 1) / 1000.0
+    fwd_avg_s = fwd_ms / max(fwd_n, 1) / 1000.0
+    bwd_tf = flops_bwd_launch / bwd_avg_s / 1e12 if bwd_n else None
+    fwd_tf = flops_fwd_launch / fwd_avg_s / 1e12 if fwd_n else None
+    peak_tf = peaks["bf16_tflops_sustained"]
+    useful_tf = 6.0 * d * V * value / 1e12
+    gtb = 2.0 * chunk * V * 2 * 2 / 1e9  # logit gradient: read e (fp16) + write G (bf16)
+    grad_gbs = gtb / (grad_ms / max(grad_n, 1) / 1000.0) if grad_n else None
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        Ts = CPU_SAMPLE_TOKENS
+        sec = cpu_oracle_sample(H, W, y, Ts)
+        cpu = {"value": Ts / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"first {Ts} of the {T} tokens (full V={V}, d={d}), float64 numpy/BLAS, one run"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["workload"], "objective": "sft", "T": T, "d": d, "V": V, "chunk": chunk,
+                   "tokens_per_gpu_per_step": T, "ignored_frac": w["frac"],
+                   "l2": "inputs larger than L2 (W 1.24 GB; chunk logits 0.62 GB per chunk)",
+                   "parallelism": f"dp{world} replicas (no collective)"},
+        "roofline": {"kernel": "k_bwd (dH and dW GEMMs of one chunk)", "bound": "tensor",
+                     "achieved": bwd_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": (bwd_tf / peak_tf) if bwd_tf else None, "traffic": None,
+                     "peak_source": f"bf16 dense, sustained, {peak_src}",
+                     "algorithmic_flops_per_launch": flops_bwd_launch, "launches": bwd_n,
+                     "avg_launch_ms": bwd_avg_s * 1e3},
+        "kernels": {
+            "k_fwd": {"achieved_tflops": fwd_tf, "avg_launch_ms": fwd_avg_s * 1e3, "launches": fwd_n,
+                      "share": fwd_ms / ms_local if ms_local else None},
+            "k_bwd": {"achieved_tflops": bwd_tf, "avg_launch_ms": bwd_avg_s * 1e3, "launches": bwd_n,
+                      "share": bwd_ms / ms_local if ms_local else None},
+            "k_grad": {"achieved_gbs": grad_gbs, "avg_launch_ms": grad_ms / max(grad_n, 1),
+                       "launches": grad_n, "share": grad_ms / ms_local if ms_local else None},
+            "other": {"ms": oth_ms, "launches": oth_n, "share": oth_ms / ms_local if ms_local else None},
+        },
+        "step_tflops_useful": useful_tf / world,
+        "pct_bf16_peak": 100.0 * useful_tf / world / peaks["bf16_tflops"],
+        "pct_bf16_peak_sustained": 100.0 * useful_tf / world / peaks["bf16_tflops_sustained"],
+        "peak_source": peak_src,
+        "peak_mem_gb": peak_mem / 1e9,
+        "unchunked_fp32_logits_gb": T * V * 4 / 1e9,
+        "e2e": {"value": e2e_tokens / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_call * args.steps,
+        "clocks": clk,
+        "loss": loss,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * sbp.h -- C ABI of the StreamBP language-model-head library (libsbp.so).
+ *
+ * The library computes the forward and backward pass of a language-model head,
+ * Z = H W^T followed by an objective on the per-token label log-probabilities,
+ * one contiguous chunk of `chunk` tokens at a time, so that only one chunk's
+ * logits and logit gradient ever exist ("StreamBP: Memory-Efficient Exact
+ * Backpropagation for Long Sequence Training of LLMs", arXiv 2506.03077; the
+ * ziziman.com article, LM-head paragraphs on SFT/GRPO and on DPO; atlas.scime.ai
+ * summary, "Approach").  Per chunk c:
+ *     Z_c  = H_c W^T                     (never more than chunk x V values)
+ *     G_c  = w_t (softmax(Z_c)_t - e_{y_t})   row by row, w_t the objective's weight
+ *     dH_c = G_c W,   dW += G_c^T H_c
+ * which is exactly the unchunked gradient (the chain rule is linear in the rows).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every array argument is a DEVICE pointer owned by the caller, except
+ *   where noted.  Base addresses must be 16-byte aligned (any cudaMalloc / PyTorch
+ *   allocation is).  The library allocates no device memory: all scratch lives in
+ *   `workspace`, of at least sbp_lmhead_workspace_bytes(...) bytes, 256-byte aligned.
+ * Layouts (row-major, dense):
+ *   H      [T, d]   dtype (bf16 or fp32)        hidden states of the T tokens
+ *   W      [V, d]   dtype                       LM-head weight
+ *   labels [T]      int32                       target of row t of H (the caller shifts);
+ *                                               == ignore_index marks an ignored token
+ *   dH     [T, d]   dtype                       always overwritten
+ *   dW     [V, d]   fp32                        overwritten (accumulate_dW = 0) or added to (1)
+ *   logp_out [T]    fp32, nullable              per-token label log-prob (0 for ignored tokens)
+ * dtype: SBP_BF16 (bf16 operands, fp32 accumulation; tcgen05 tensor cores) or
+ *   SBP_FP32 (fp32 operands and arithmetic, no TF32).
+ * Sizes: T >= 0, d >= 1, V >= 1, chunk >= 1.  For SBP_BF16, d and V must be
+ *   multiples of 8 (16-byte rows for the tensor-memory-access unit).
+ * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *   only enqueues work on it and returns; nothing synchronises the host.  Calls on
+ *   different streams need distinct workspaces.
+ * Errors: the return value is an sbp_status.  Argument errors are found on the host
+ *   and returned before anything is enqueued (outputs untouched).  Errors only the
+ *   device can see (a label outside [0, V) other than ignore_index; a pipeline wait
+ *   that ran past its time limit) are written to *dev_status (device int32, zeroed by
+ *   the call at enqueue); read it after synchronising.  After a device error the
+ *   outputs are undefined.  No call traps the device.
+ * Reductions: the mean denominators are over the whole call, never per chunk.
+ *   N = number of tokens with labels[t] != ignore_index.  When N = 0 the loss is 0
+ *   and the gradients are 0.
+ */
+#ifndef SBP_H_
+#define SBP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define SBP_OK 0
+#define SBP_ERR_INVALID_ARG 1   /* null pointer, negative or zero size, bad dtype/mode   */
+#define SBP_ERR_ALIGNMENT 2     /* pointer or row stride not aligned as required          */
+#define SBP_ERR_WORKSPACE 3     /* workspace too small or not 256-byte aligned            */
+#define SBP_ERR_LABEL_RANGE 4   /* (device) a label outside [0, V) and != ignore_index    */
+#define SBP_ERR_TIMEOUT 5       /* (device) a kernel pipeline wait exceeded its limit      */
+#define SBP_ERR_CUDA 6          /* a CUDA runtime call failed (launch, memset, ...)       */
+#define SBP_ERR_UNSUPPORTED 7   /* shape the kernels do not handle (see dtype rules)       */
+
+/* operand dtypes */
+#define SBP_BF16 0
+#define SBP_FP32 1
+
+/* workspace modes */
+#define SBP_MODE_SFT 0
+#define SBP_MODE_GRPO 1
+#define SBP_MODE_DPO1 2
+#define SBP_MODE_DPO2 3
+
+/* Bytes of workspace the call with these arguments needs.  It depends on T only
+ * through O(T) scalars; the bulk is one chunk's logits/gradient (chunk x V) plus
+ * chunk x d split partials.  Returns 0 for invalid arguments. */
+size_t sbp_lmhead_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t chunk,
+                                  int dtype, int mode);
+
+/* SFT cross-entropy (ziziman.com article, LM-head paragraph on SFT/GRPO):
+ *   L = -(1/N) sum_{t: y_t != ign} logp_t,   logp_t = Z_{t,y_t} - logsumexp_v Z_{t,v}.
+ * Outputs: *loss (device fp32), *n_valid (device int64, = N), logp_out (nullable),
+ * dH = dL/dH, dW (+)= dL/dW. */
+int sbp_lmhead_sft(const void* H, const void* W, const int32_t* labels,
+                   int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                   int dtype, float* loss, int64_t* n_valid, float* logp_out,
+                   void* dH, float* dW, int accumulate_dW,
+                   void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* GRPO / PPO-clip per-token objective (ziziman.com article: GRPO shares the
+ * per-position independence of SFT), mean over the N non-ignored tokens:
+ *   r_t = exp(logp_t - logp_old_t),
+ *   L = -(1/N) sum_t min(r_t A_t, clip(r_t, clip_lo, clip_hi) A_t).
+ * advantages [T] fp32 (per-token A_t; broadcast per response by the caller),
+ * logp_old [T] fp32.  The subgradient at the clip edges takes the unclipped branch
+ * (closed interval).  Other arguments as sbp_lmhead_sft. */
+int sbp_lmhead_grpo(const void* H, const void* W, const int32_t* labels,
+                    const float* advantages, const float* logp_old,
+                    float clip_lo, float clip_hi,
+                    int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                    int dtype, float* loss, int64_t* n_valid, float* logp_out,
+                    void* dH, float* dW, int accumulate_dW,
+                    void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* DPO, first pass (ziziman.com article, DPO paragraph: the sigmoid couples the
+ * positions, so the per-sequence sums are formed first).  Sequences are the token
+ * ranges [cu_seqlens[i], cu_seqlens[i+1]), i < n_seq (cu_seqlens: device int32
+ * [n_seq+1], non-decreasing, within [0, T]).
+ *   seq_logp[i] = sum_{t in seq i, y_t != ign} logp_t      (device fp64 [n_seq])
+ * No gradient.  logp_out and n_valid are nullable. */
+int sbp_lmhead_dpo_pass1(const void* H, const void* W, const int32_t* labels,
+                         const int32_t* cu_seqlens, int32_t n_seq,
+                         int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                         int dtype, double* seq_logp, float* logp_out, int64_t* n_valid,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* DPO, second pass: sequences [0, P) are the chosen answers and [P, 2P) the
+ * rejected ones (n_seq = 2P); pair i = (i, i+P).
+ *   m_i = beta [(S_i - Sref_i) - (S_{i+P} - Sref_{i+P})],   L = (1/P) sum_i softplus(-m_i)
+ * and the logit gradient of a token of sequence j is w_j (softmax - onehot) with
+ * w_i = beta sigma(-m_i)/P (chosen), w_{i+P} = -beta sigma(-m_i)/P (rejected): the
+ * gradient is again independent per position once the sums are known (DPO
+ * paragraph).  seq_logp / ref_seq_logp: device fp64 [n_seq]; margins: device fp64 [P],
+ * nullable.  Outputs *loss, dH, dW as sbp_lmhead_sft. */
+int sbp_lmhead_dpo_pass2(const void* H, const void* W, const int32_t* labels,
+                         const int32_t* cu_seqlens, int32_t n_seq,
+                         const double* seq_logp, const double* ref_seq_logp, float beta,
+                         int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                         int dtype, float* loss, double* margins,
+                         void* dH, float* dW, int accumulate_dW,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Kernel timing (a profiling aid; off by default).  While enabled, every call records
+ * a pair of CUDA events on its stream around each launch of the kernels below, per
+ * kernel class:
+ *   0 forward GEMM + row statistics   1 backward GEMMs (dH and dW)
+ *   2 logit gradient                  3 everything else (scan, combine, reductions)
+ * sbp_profile_read() waits for the recorded events, adds their durations to
+ * ms[class] and the launch counts to launches[class] for class < n, clears the record
+ * and returns the number of pairs read (or -SBP_ERR_CUDA).  Host-thread local.
+ * Events are created once and reused; no device memory is allocated. */
+int sbp_profile_enable(int on);
+int sbp_profile_read(double* ms, int64_t* launches, int n);
+
+/* Human-readable name of a status code (static storage). */
+const char* sbp_status_string(int status);
+
+/* Number of kernel launches the last successful call on this host thread enqueued. */
+int sbp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SBP_H_ */

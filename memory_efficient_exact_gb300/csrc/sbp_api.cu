@@ -1,0 +1,700 @@
+// C ABI of libsbp.so and the host-side chunk scheduler.
+//
+// One call = label scan, then for each chunk of `chunk` rows (the chunk loop of the
+// StreamBP LM head: ziziman.com article, LM-head paragraphs):
+//   forward GEMM + row-statistics epilogue -> combine (lse, logp, weight) ->
+//   logit gradient (in place over the chunk buffer) -> dH / dW GEMMs -> dH reduce,
+// and finally the deterministic loss reduction.  Everything is enqueued on the
+// caller's stream; nothing here synchronises the host or allocates device memory.
+#include <cfloat>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "sbp_internal.h"
+
+namespace sbp {
+
+static thread_local int g_launches = 0;
+
+// ---- optional per-kernel-class timing (CUDA events on the call's stream) ----
+namespace prof {
+constexpr int kClasses = 4;
+struct Pair { cudaEvent_t a, b; int cls; };
+static thread_local bool g_on = false;
+static thread_local std::vector<Pair>* g_pairs = nullptr;   // recorded, not yet read
+static thread_local std::vector<cudaEvent_t>* g_pool = nullptr;
+
+static cudaEvent_t get_event() {
+  if (!g_pool) g_pool = new std::vector<cudaEvent_t>();
+  if (!g_pool->empty()) {
+    cudaEvent_t e = g_pool->back();
+    g_pool->pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+struct Scope {
+  cudaEvent_t a = nullptr, b = nullptr;
+  int cls;
+  cudaStream_t s;
+  Scope(int c, cudaStream_t st) : cls(c), s(st) {
+    if (!g_on) return;
+    a = get_event();
+    b = get_event();
+    if (a && b) cudaEventRecord(a, s);
+  }
+  ~Scope() {
+    if (!g_on || !a || !b) return;
+    cudaEventRecord(b, s);
+    if (!g_pairs) g_pairs = new std::vector<Pair>();
+    g_pairs->push_back({a, b, cls});
+  }
+};
+}  // namespace prof
+
+static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// Split-K factor for dH: the backward kernel schedules the dH units (K = V, long)
+// before the dW units (K = rows, short) from one dynamic queue.  One dH unit should
+// stay below a quarter of the average per-SM work so the short dW units can even
+// out the finish times.
+int choose_splits(int64_t rows, int64_t d, int64_t V, int sms) {
+  const int64_t mt_c = (rows + 127) / 128, nt_d = (d + 255) / 256, kb_v = (V + 63) / 64;
+  const int64_t mt_v = (V + 127) / 128, kb_c = (rows + 63) / 64;
+  const double total = double(mt_c * nt_d * kb_v + mt_v * nt_d * kb_c);
+  const double per_sm = total / double(sms > 0 ? sms : 148);
+  int s = (int)std::ceil(4.0 * double(kb_v) / (per_sm > 1.0 ? per_sm : 1.0));
+  if (s < 1) s = 1;
+  if (s > 16) s = 16;
+  if (s > kb_v) s = (int)kb_v;
+  return s;
+}
+
+bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L) {
+  if (T < 0 || d < 1 || V < 1 || chunk < 1 || chunk > 65535) return false;
+  if (dtype != SBP_BF16 && dtype != SBP_FP32) return false;
+  if (mode < SBP_MODE_SFT || mode > SBP_MODE_DPO2) return false;
+  Layout l;
+  l.T = T; l.d = d; l.V = V; l.dtype = dtype; l.mode = mode;
+  l.chunk = T > 0 ? (chunk < T ? chunk : T) : 1;
+  l.esize = dtype == SBP_BF16 ? 2 : 4;
+  l.ldv = dtype == SBP_BF16 ? ((V + 63) / 64) * 64 : ((V + 3) / 4) * 4;
+  l.ntiles = (V + kStatW - 1) / kStatW;
+  l.splits = dtype == SBP_BF16 ? choose_splits(l.chunk, d, V, num_sms()) : 1;
+  l.n_chunks = T > 0 ? (T + l.chunk - 1) / l.chunk : 0;
+  l.max_seq = T + 64;
+  size_t o = 0;
+  l.off_zg = o;      o = align256(o + (size_t)l.chunk * l.ldv * l.esize);
+  l.off_part = o;    o = align256(o + (size_t)l.chunk * l.ntiles * sizeof(float2));
+  l.off_zy = o;      o = align256(o + (size_t)l.chunk * sizeof(float));
+  l.off_rowv = o;    o = align256(o + (size_t)l.chunk * sizeof(float));
+  l.off_dhp = o;     o = align256(o + (size_t)l.splits * l.chunk * d * sizeof(float));
+  l.off_tokloss = o; o = align256(o + (size_t)(T + 1) * sizeof(float));
+  l.off_logp = o;    o = align256(o + (size_t)(T + 1) * sizeof(float));
+  l.off_seqw = o;    o = align256(o + (size_t)l.max_seq * sizeof(float));
+  l.off_scal = o;    o = align256(o + 64);  // [0] int64 N
+  l.off_cnt = o;     o = align256(o + (size_t)(l.n_chunks + 1) * sizeof(uint32_t));
+  l.total = o;
+  *L = l;
+  return true;
+}
+
+namespace {
+
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Label scan (one block): N = #{t : y_t != ign}; labels outside [0, V) other than
+// ign raise SBP_ERR_LABEL_RANGE; zeroes the per-chunk scheduler counters.
+__global__ void __launch_bounds__(1024) k_prep(const int32_t* __restrict__ y, int64_t T, int64_t V, int32_t ign,
+                                               long long* __restrict__ nvalid, uint32_t* __restrict__ counters,
+                                               int64_t n_counters, int32_t* status) {
+  __shared__ long long red[32];
+  long long c = 0;
+  bool bad = false;
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
+    const int32_t v = y[t];
+    if (v != ign) {
+      ++c;
+      if (v < 0 || (int64_t)v >= V) bad = true;
+    }
+  }
+  for (int64_t i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
+  if (bad) set_status(status, SBP_ERR_LABEL_RANGE);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long s = 0;
+    for (int i = 0; i < (int)(blockDim.x / 32); ++i) s += red[i];
+    *nvalid = s;
+  }
+}
+
+struct CombineArgs {
+  const float2* part; int64_t ntiles;
+  const float* zy;
+  const int32_t* labels;   // chunk-offset
+  int rows; int64_t r0; int64_t V; int32_t ign;
+  const long long* nvalid;
+  float* w_row;            // [rows] weight of the row's logit gradient
+  float* logp;             // [T]
+  float* tokloss;          // [T] loss contribution of the token
+  // GRPO
+  const float* adv; const float* logp_old; float clip_lo, clip_hi;
+  // DPO pass 2
+  const int32_t* cu; int n_seq; const float* seqw;
+};
+
+// One warp per row: lse = M + log sum_i s_i exp(m_i - M) over the row's tile partials,
+// logp = z_y - lse, then the objective's weight w and loss term.  The tile maxima are
+// replaced in place by the gradient scales w exp(m_i - lse), so that the gradient
+// kernel needs one multiply per element: G = e * scale - w [v = y].
+template <int MODE>
+__global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
+  const int lane = threadIdx.x % 32;
+  const int row = blockIdx.x * 8 + threadIdx.x / 32;
+  if (row >= a.rows) return;
+  float2* p = const_cast<float2*>(a.part) + (int64_t)row * a.ntiles;
+  float m = -FLT_MAX;
+  for (int64_t i = lane; i < a.ntiles; i += 32) m = fmaxf(m, p[i].x);
+  m = warp_max(m);
+  float s = 0.f;
+  for (int64_t i = lane; i < a.ntiles; i += 32) {
+    const float2 q = p[i];
+    s += q.y * expf(q.x - m);
+  }
+  s = warp_sum(s);
+  const float lse = m + logf(s);
+  const int32_t y = a.labels[row];
+  const bool valid = y != a.ign && y >= 0 && (int64_t)y < a.V;
+  const float logp = valid ? a.zy[row] - lse : 0.f;
+  const long long N = *a.nvalid;
+  const float invN = N > 0 ? (float)(1.0 / (double)N) : 0.f;
+  float w = 0.f, tl = 0.f;
+  const int64_t t = a.r0 + row;
+  if (MODE == SBP_MODE_SFT) {
+    w = valid ? invN : 0.f;
+    tl = valid ? -logp * invN : 0.f;
+  } else if (MODE == SBP_MODE_GRPO) {
+    if (valid) {
+      const float A = a.adv[t];
+      const float r = expf(logp - a.logp_old[t]);
+      const float rc = fminf(fmaxf(r, a.clip_lo), a.clip_hi);
+      const float o = fminf(r * A, rc * A);
+      const bool g = (A >= 0.f) ? (r <= a.clip_hi) : (r >= a.clip_lo);
+      w = g ? A * r * invN : 0.f;
+      tl = -o * invN;
+    }
+  } else if (MODE == SBP_MODE_DPO2) {
+    if (valid && a.n_seq > 0 && t >= a.cu[0] && t < a.cu[a.n_seq]) {
+      int lo = 0, hi = a.n_seq - 1;  // last i with cu[i] <= t
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (a.cu[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      w = a.seqw[lo];
+    }
+  }
+  for (int64_t i = lane; i < a.ntiles; i += 32) p[i].x = w * expf(p[i].x - lse);
+  if (lane == 0) {
+    a.w_row[row] = w;
+    a.logp[t] = logp;
+    a.tokloss[t] = tl;
+  }
+}
+
+__device__ __forceinline__ void load8(const __half* p, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __half22float2(h[i]);
+    f[2 * i] = x.x; f[2 * i + 1] = x.y;
+  }
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* f) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void load8(const float* p, float* f) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float* f) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+__device__ __forceinline__ float ld1(const __half* p) { return __half2float(*p); }
+__device__ __forceinline__ float ld1(const float* p) { return *p; }
+__device__ __forceinline__ void st1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void st1(float* p, float v) { *p = v; }
+
+// Logit gradient of one chunk, in place over the chunk buffer:
+//   G[r, v] = e[r, v] * scale[r, tile(v)] - w_r [v = y_r]   (= w_r (softmax - onehot)).
+// TE -> TG: fp16 -> bf16 (tensor-core path) or fp32 -> fp32 (SIMT path).
+template <typename TE, typename TG>
+__global__ void __launch_bounds__(256) k_grad(void* buf, int64_t ld, int64_t V, const float2* __restrict__ part,
+                                              int64_t ntiles, const float* __restrict__ w_row,
+                                              const int32_t* __restrict__ labels) {
+  static_assert(sizeof(TE) == sizeof(TG), "in-place conversion needs equal element sizes");
+  const int64_t row = blockIdx.y;
+  const float w = w_row[row];
+  const int32_t y = labels[row];
+  TE* e = reinterpret_cast<TE*>(buf) + row * ld;
+  TG* g = reinterpret_cast<TG*>(buf) + row * ld;
+  const float2* sc = part + row * ntiles;
+  for (int64_t v0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; v0 < V;
+       v0 += (int64_t)gridDim.x * blockDim.x * 8) {
+    float f[8];
+    if (v0 + 8 <= V) {
+      if (w == 0.f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+      } else {
+        load8(e + v0, f);
+        const float s = sc[v0 / kStatW].x;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] *= s;
+        if (y >= v0 && y < v0 + 8) f[y - v0] -= w;
+      }
+      store8(g + v0, f);
+    } else {
+      for (int64_t v = v0; v < V; ++v) {
+        float x = w == 0.f ? 0.f : ld1(e + v) * sc[v / kStatW].x - (v == y ? w : 0.f);
+        st1(g + v, x);
+      }
+    }
+  }
+}
+
+// dH rows of the chunk = sum over the split-K partials, converted to the output dtype.
+template <typename TO>
+__global__ void __launch_bounds__(256) k_dh_reduce(const float* __restrict__ part, int splits, int64_t n,
+                                                   int64_t plane, TO* __restrict__ out) {
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n;
+       i += (int64_t)gridDim.x * blockDim.x * 4) {
+    if (i + 4 <= n) {
+      float4 acc = *reinterpret_cast<const float4*>(part + i);
+      for (int s = 1; s < splits; ++s) {
+        const float4 q = *reinterpret_cast<const float4*>(part + s * plane + i);
+        acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+      }
+      st1(out + i, acc.x); st1(out + i + 1, acc.y); st1(out + i + 2, acc.z); st1(out + i + 3, acc.w);
+    } else {
+      for (int64_t j = i; j < n; ++j) {
+        float acc = part[j];
+        for (int s = 1; s < splits; ++s) acc += part[s * plane + j];
+        st1(out + j, acc);
+      }
+    }
+  }
+}
+
+// Deterministic loss reduction (one block, fp64, fixed order).
+__global__ void __launch_bounds__(1024) k_loss_final(const float* __restrict__ tokloss, int64_t T,
+                                                     const long long* __restrict__ nvalid_ws, float* loss,
+                                                     int64_t* n_valid_out) {
+  __shared__ double red[1024];
+  double acc = 0.0;
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) acc += (double)tokloss[t];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (loss) *loss = (float)red[0];
+    if (n_valid_out) *n_valid_out = (int64_t)*nvalid_ws;
+  }
+}
+
+// DPO pass 1: S_i = sum of logp over [cu[i], cu[i+1]) (one block per sequence, fp64).
+__global__ void __launch_bounds__(256) k_seq_sums(const float* __restrict__ logp, const int32_t* __restrict__ cu,
+                                                  double* __restrict__ seq_logp) {
+  __shared__ double red[256];
+  const int i = blockIdx.x;
+  const int64_t b = cu[i], e = cu[i + 1];
+  double acc = 0.0;
+  for (int64_t t = b + threadIdx.x; t < e; t += blockDim.x) acc += (double)logp[t];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) seq_logp[i] = red[0];
+}
+
+__device__ __forceinline__ double softplus_d(double x) {
+  return (x > 0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+__device__ __forceinline__ double sigmoid_d(double x) {
+  if (x >= 0) return 1.0 / (1.0 + exp(-x));
+  const double e = exp(x);
+  return e / (1.0 + e);
+}
+
+// DPO pass 2 prologue (one thread): margins, loss and per-sequence weights.
+__global__ void k_dpo_scales(const double* __restrict__ S, const double* __restrict__ R, int n_seq, double beta,
+                             float* loss, double* margins, float* seqw) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const int P = n_seq / 2;
+  double L = 0.0;
+  for (int i = 0; i < P; ++i) {
+    const double m = beta * ((S[i] - R[i]) - (S[i + P] - R[i + P]));
+    L += softplus_d(-m);
+    const double w = beta * sigmoid_d(-m) / (double)P;
+    seqw[i] = (float)w;
+    seqw[i + P] = (float)(-w);
+    if (margins) margins[i] = m;
+  }
+  if (loss) *loss = P > 0 ? (float)(L / (double)P) : 0.f;
+}
+
+__global__ void k_zero_f32(float* p, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0.f;
+}
+
+inline unsigned grid_for(int64_t work, int threads, int64_t cap = 4096) {
+  int64_t g = (work + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (unsigned)g;
+}
+
+struct Call {
+  int mode;
+  const void* H; const void* W; const int32_t* labels;
+  int64_t T, d, V, chunk; int32_t ign; int dtype;
+  // SFT / GRPO / DPO2 outputs
+  float* loss; int64_t* n_valid; float* logp_out;
+  void* dH; float* dW; int accumulate_dW;
+  // GRPO
+  const float* adv; const float* logp_old; float clip_lo, clip_hi;
+  // DPO
+  const int32_t* cu; int n_seq; double* seq_logp; const double* seq_in; const double* ref_in;
+  float beta; double* margins;
+  void* ws; size_t ws_bytes; int32_t* dev_status; cudaStream_t stream;
+};
+
+#define SBP_CUDA(x)                        \
+  do {                                     \
+    cudaError_t e_ = (x);                  \
+    if (e_ != cudaSuccess) return SBP_ERR_CUDA; \
+  } while (0)
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const Call& c, Layout* L) {
+  if (!make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, L)) return SBP_ERR_INVALID_ARG;
+  if (c.T > 0 && (!c.H || !c.labels)) return SBP_ERR_INVALID_ARG;
+  if (!c.W || !c.dev_status) return SBP_ERR_INVALID_ARG;
+  if (c.T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
+  const bool grad = c.mode != SBP_MODE_DPO1;
+  if (grad && !c.dW) return SBP_ERR_INVALID_ARG;
+  if (grad && c.T > 0 && !c.dH) return SBP_ERR_INVALID_ARG;
+  if (c.mode == SBP_MODE_GRPO && c.T > 0 && (!c.adv || !c.logp_old)) return SBP_ERR_INVALID_ARG;
+  if (c.mode == SBP_MODE_GRPO && !(c.clip_lo <= c.clip_hi)) return SBP_ERR_INVALID_ARG;
+  if (c.mode == SBP_MODE_DPO1 || c.mode == SBP_MODE_DPO2) {
+    if (c.n_seq < 0 || c.n_seq > L->max_seq || (c.n_seq > 0 && !c.cu)) return SBP_ERR_INVALID_ARG;
+    if (c.mode == SBP_MODE_DPO1 && c.n_seq > 0 && !c.seq_logp) return SBP_ERR_INVALID_ARG;
+    if (c.mode == SBP_MODE_DPO2 && (c.n_seq % 2 != 0 || (c.n_seq > 0 && (!c.seq_in || !c.ref_in))))
+      return SBP_ERR_INVALID_ARG;
+  }
+  if (c.dtype == SBP_BF16 && (c.d % 8 != 0 || c.V % 8 != 0)) return SBP_ERR_UNSUPPORTED;
+  if ((c.H && !al16(c.H)) || !al16(c.W) || (c.dH && !al16(c.dH)) || (c.dW && !al16(c.dW)))
+    return SBP_ERR_ALIGNMENT;
+  if (c.dtype == SBP_FP32 && c.d % 4 != 0 && c.dH) {
+    // fp32 dH rows are written 4 at a time only when d % 4 == 0; other d take the
+    // scalar tail path, which needs no alignment beyond the element size.
+  }
+  if (!c.ws || (reinterpret_cast<uintptr_t>(c.ws) & 255u) || c.ws_bytes < L->total) return SBP_ERR_WORKSPACE;
+  return SBP_OK;
+}
+
+int run(const Call& c) {
+  Layout L;
+  int st = validate(c, &L);
+  if (st != SBP_OK) return st;
+  cudaStream_t s = c.stream;
+  char* ws = static_cast<char*>(c.ws);
+  void* zg = ws + L.off_zg;
+  float2* part = reinterpret_cast<float2*>(ws + L.off_part);
+  float* zy = reinterpret_cast<float*>(ws + L.off_zy);
+  float* w_row = reinterpret_cast<float*>(ws + L.off_rowv);
+  float* dhp = reinterpret_cast<float*>(ws + L.off_dhp);
+  float* tokloss = reinterpret_cast<float*>(ws + L.off_tokloss);
+  float* logp = reinterpret_cast<float*>(ws + L.off_logp);
+  float* seqw = reinterpret_cast<float*>(ws + L.off_seqw);
+  long long* nvalid = reinterpret_cast<long long*>(ws + L.off_scal);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + L.off_cnt);
+  int launches = 0;
+
+  SBP_CUDA(cudaMemsetAsync(c.dev_status, 0, sizeof(int32_t), s));
+  {
+    prof::Scope ps(3, s);
+    k_prep<<<1, 1024, 0, s>>>(c.labels, c.T, c.V, c.ign, nvalid, counters, L.n_chunks + 1, c.dev_status);
+  }
+  ++launches;
+  SBP_CUDA(cudaGetLastError());
+
+  const bool grad = c.mode != SBP_MODE_DPO1;
+  if (c.mode == SBP_MODE_DPO2) {
+    k_dpo_scales<<<1, 32, 0, s>>>(c.seq_in, c.ref_in, c.n_seq, (double)c.beta, c.loss, c.margins, seqw);
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+  }
+  if (grad && c.T == 0 && !c.accumulate_dW) {
+    k_zero_f32<<<grid_for(c.V * c.d, 256), 256, 0, s>>>(c.dW, c.V * c.d);
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+  }
+
+  const bool bf16 = c.dtype == SBP_BF16;
+  const size_t es = bf16 ? 2 : 4;
+  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+    const int64_t r0 = ci * L.chunk;
+    const int rows = (int)((r0 + L.chunk <= c.T) ? L.chunk : c.T - r0);
+    const int32_t* yl = c.labels + r0;
+    // forward GEMM + row statistics
+    if (bf16) {
+      TcFwdArgs a{};
+      a.H = c.H; a.W = c.W; a.T = c.T; a.d = c.d; a.V = c.V; a.r0 = r0; a.rows = rows;
+      a.labels = yl; a.ignore_index = c.ign;
+      a.E = grad ? zg : nullptr; a.lde = L.ldv; a.part = part; a.zy = zy; a.status = c.dev_status;
+      prof::Scope ps(0, s);
+      SBP_CUDA(tc_forward(a, s));
+      ++launches;
+    } else {
+      prof::Scope ps(0, s);
+      SBP_CUDA(simt_forward(static_cast<const float*>(c.H), static_cast<const float*>(c.W), c.d, c.V, r0, rows,
+                            yl, c.ign, static_cast<float*>(zg), L.ldv, part, zy, grad, s));
+      launches += 2;
+    }
+    // combine: lse, logp, weights, loss terms
+    CombineArgs ca{};
+    ca.part = part; ca.ntiles = L.ntiles; ca.zy = zy; ca.labels = yl; ca.rows = rows; ca.r0 = r0;
+    ca.V = c.V; ca.ign = c.ign; ca.nvalid = nvalid; ca.w_row = w_row; ca.logp = logp; ca.tokloss = tokloss;
+    ca.adv = c.adv; ca.logp_old = c.logp_old; ca.clip_lo = c.clip_lo; ca.clip_hi = c.clip_hi;
+    ca.cu = c.cu; ca.n_seq = c.n_seq; ca.seqw = seqw;
+    const unsigned gc = (unsigned)((rows + 7) / 8);
+    {
+    prof::Scope ps(3, s);
+    switch (c.mode) {
+      case SBP_MODE_SFT: k_combine<SBP_MODE_SFT><<<gc, 256, 0, s>>>(ca); break;
+      case SBP_MODE_GRPO: k_combine<SBP_MODE_GRPO><<<gc, 256, 0, s>>>(ca); break;
+      case SBP_MODE_DPO1: k_combine<SBP_MODE_DPO1><<<gc, 256, 0, s>>>(ca); break;
+      default: k_combine<SBP_MODE_DPO2><<<gc, 256, 0, s>>>(ca); break;
+    }
+    }
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+    if (!grad) continue;
+    // logit gradient, in place
+    {
+      const int64_t vec = (c.V + 7) / 8;
+      dim3 g((unsigned)((vec + 255) / 256), (unsigned)rows);
+      prof::Scope ps(2, s);
+      if (bf16) k_grad<__half, __nv_bfloat16><<<g, 256, 0, s>>>(zg, L.ldv, c.V, part, L.ntiles, w_row, yl);
+      else k_grad<float, float><<<g, 256, 0, s>>>(zg, L.ldv, c.V, part, L.ntiles, w_row, yl);
+      ++launches;
+      SBP_CUDA(cudaGetLastError());
+    }
+    // dH_c = G_c W and dW (+)= G_c^T H_c
+    const int dw_acc = (ci > 0 || c.accumulate_dW) ? 1 : 0;
+    int splits = 1;
+    if (bf16) {
+      TcBwdArgs b{};
+      b.G = zg; b.ldg = L.ldv; b.H = c.H; b.W = c.W; b.T = c.T; b.d = c.d; b.V = c.V;
+      b.r0 = r0; b.rows = rows;
+      splits = choose_splits(rows, c.d, c.V, num_sms());
+      if (splits > L.splits) splits = L.splits;
+      b.splits = splits; b.dh_part = dhp; b.dW = c.dW; b.dw_accumulate = dw_acc;
+      b.counter = counters + ci; b.status = c.dev_status;
+      prof::Scope ps(1, s);
+      SBP_CUDA(tc_backward(b, s));
+      ++launches;
+    } else {
+      prof::Scope ps(1, s);
+      SBP_CUDA(simt_backward(static_cast<const float*>(zg), L.ldv, static_cast<const float*>(c.H),
+                             static_cast<const float*>(c.W), c.d, c.V, r0, rows, dhp, c.dW, dw_acc, s));
+      launches += 2;
+    }
+    const int64_t n = (int64_t)rows * c.d;
+    prof::Scope ps(3, s);
+    if (bf16)
+      k_dh_reduce<__nv_bfloat16><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
+          dhp, splits, n, (int64_t)rows * c.d, static_cast<__nv_bfloat16*>(c.dH) + r0 * c.d);
+    else
+      k_dh_reduce<float><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
+          dhp, splits, n, (int64_t)rows * c.d, static_cast<float*>(c.dH) + r0 * c.d);
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+  }
+
+  if (c.mode == SBP_MODE_SFT || c.mode == SBP_MODE_GRPO) {
+    k_loss_final<<<1, 1024, 0, s>>>(tokloss, c.T, nvalid, c.loss, c.n_valid);
+    ++launches;
+  } else if (c.mode == SBP_MODE_DPO1) {
+    if (c.n_seq > 0) {
+      k_seq_sums<<<c.n_seq, 256, 0, s>>>(logp, c.cu, c.seq_logp);
+      ++launches;
+    }
+    if (c.n_valid) {
+      k_loss_final<<<1, 1024, 0, s>>>(tokloss, 0, nvalid, nullptr, c.n_valid);
+      ++launches;
+    }
+  }
+  SBP_CUDA(cudaGetLastError());
+  if (c.logp_out && c.T > 0)
+    SBP_CUDA(cudaMemcpyAsync(c.logp_out, logp, (size_t)c.T * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  g_launches = launches;
+  (void)es;
+  return SBP_OK;
+}
+
+}  // namespace
+}  // namespace sbp
+
+using namespace sbp;
+
+extern "C" {
+
+size_t sbp_lmhead_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode) {
+  Layout L;
+  if (!make_layout(T, d, V, chunk, dtype, mode, &L)) return 0;
+  return L.total;
+}
+
+int sbp_lmhead_sft(const void* H, const void* W, const int32_t* labels, int64_t T, int64_t d, int64_t V,
+                   int64_t chunk, int32_t ignore_index, int dtype, float* loss, int64_t* n_valid,
+                   float* logp_out, void* dH, float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                   int32_t* dev_status, void* stream) {
+  if (!loss) return SBP_ERR_INVALID_ARG;
+  Call c{};
+  c.mode = SBP_MODE_SFT; c.H = H; c.W = W; c.labels = labels; c.T = T; c.d = d; c.V = V; c.chunk = chunk;
+  c.ign = ignore_index; c.dtype = dtype; c.loss = loss; c.n_valid = n_valid; c.logp_out = logp_out;
+  c.dH = dH; c.dW = dW; c.accumulate_dW = accumulate_dW; c.ws = workspace; c.ws_bytes = ws_bytes;
+  c.dev_status = dev_status; c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int sbp_lmhead_grpo(const void* H, const void* W, const int32_t* labels, const float* advantages,
+                    const float* logp_old, float clip_lo, float clip_hi, int64_t T, int64_t d, int64_t V,
+                    int64_t chunk, int32_t ignore_index, int dtype, float* loss, int64_t* n_valid,
+                    float* logp_out, void* dH, float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                    int32_t* dev_status, void* stream) {
+  if (!loss) return SBP_ERR_INVALID_ARG;
+  Call c{};
+  c.mode = SBP_MODE_GRPO; c.H = H; c.W = W; c.labels = labels; c.T = T; c.d = d; c.V = V; c.chunk = chunk;
+  c.ign = ignore_index; c.dtype = dtype; c.loss = loss; c.n_valid = n_valid; c.logp_out = logp_out;
+  c.dH = dH; c.dW = dW; c.accumulate_dW = accumulate_dW; c.adv = advantages; c.logp_old = logp_old;
+  c.clip_lo = clip_lo; c.clip_hi = clip_hi; c.ws = workspace; c.ws_bytes = ws_bytes;
+  c.dev_status = dev_status; c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int sbp_lmhead_dpo_pass1(const void* H, const void* W, const int32_t* labels, const int32_t* cu_seqlens,
+                         int32_t n_seq, int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                         int dtype, double* seq_logp, float* logp_out, int64_t* n_valid, void* workspace,
+                         size_t ws_bytes, int32_t* dev_status, void* stream) {
+  Call c{};
+  c.mode = SBP_MODE_DPO1; c.H = H; c.W = W; c.labels = labels; c.T = T; c.d = d; c.V = V; c.chunk = chunk;
+  c.ign = ignore_index; c.dtype = dtype; c.cu = cu_seqlens; c.n_seq = n_seq; c.seq_logp = seq_logp;
+  c.logp_out = logp_out; c.n_valid = n_valid; c.ws = workspace; c.ws_bytes = ws_bytes;
+  c.dev_status = dev_status; c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int sbp_lmhead_dpo_pass2(const void* H, const void* W, const int32_t* labels, const int32_t* cu_seqlens,
+                         int32_t n_seq, const double* seq_logp, const double* ref_seq_logp, float beta,
+                         int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index, int dtype,
+                         float* loss, double* margins, void* dH, float* dW, int accumulate_dW,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!loss) return SBP_ERR_INVALID_ARG;
+  Call c{};
+  c.mode = SBP_MODE_DPO2; c.H = H; c.W = W; c.labels = labels; c.T = T; c.d = d; c.V = V; c.chunk = chunk;
+  c.ign = ignore_index; c.dtype = dtype; c.cu = cu_seqlens; c.n_seq = n_seq; c.seq_in = seq_logp;
+  c.ref_in = ref_seq_logp; c.beta = beta; c.loss = loss; c.margins = margins; c.dH = dH; c.dW = dW;
+  c.accumulate_dW = accumulate_dW; c.ws = workspace; c.ws_bytes = ws_bytes; c.dev_status = dev_status;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+const char* sbp_status_string(int status) {
+  switch (status) {
+    case SBP_OK: return "SBP_OK";
+    case SBP_ERR_INVALID_ARG: return "SBP_ERR_INVALID_ARG";
+    case SBP_ERR_ALIGNMENT: return "SBP_ERR_ALIGNMENT";
+    case SBP_ERR_WORKSPACE: return "SBP_ERR_WORKSPACE";
+    case SBP_ERR_LABEL_RANGE: return "SBP_ERR_LABEL_RANGE";
+    case SBP_ERR_TIMEOUT: return "SBP_ERR_TIMEOUT";
+    case SBP_ERR_CUDA: return "SBP_ERR_CUDA";
+    case SBP_ERR_UNSUPPORTED: return "SBP_ERR_UNSUPPORTED";
+    default: return "SBP_ERR_UNKNOWN";
+  }
+}
+
+int sbp_last_launch_count(void) { return g_launches; }
+
+int sbp_profile_enable(int on) {
+  prof::g_on = on != 0;
+  return SBP_OK;
+}
+
+int sbp_profile_read(double* ms, int64_t* launches, int n) {
+  if (!prof::g_pairs) return 0;
+  int cnt = 0;
+  int err = 0;
+  for (auto& p : *prof::g_pairs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&t, p.a, p.b) != cudaSuccess) err = 1;
+    if (p.cls < n) {
+      if (ms) ms[p.cls] += (double)t;
+      if (launches) launches[p.cls] += 1;
+    }
+    if (!prof::g_pool) prof::g_pool = new std::vector<cudaEvent_t>();
+    prof::g_pool->push_back(p.a);
+    prof::g_pool->push_back(p.b);
+    ++cnt;
+  }
+  prof::g_pairs->clear();
+  return err ? -SBP_ERR_CUDA : cnt;
+}
+
+}  // extern "C"

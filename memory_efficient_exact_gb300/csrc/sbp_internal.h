@@ -1,0 +1,71 @@
+// Internal declarations shared by the translation units of libsbp.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/sbp.h"
+
+namespace sbp {
+
+// Width (in vocabulary columns) of one row-statistics tile: each (row, tile) pair gets
+// one partial (max, sum of exp) and one gradient scale.
+constexpr int kStatW = 128;
+
+// Workspace carve-up.  Every region starts on a 256-byte boundary.
+struct Layout {
+  int64_t T = 0, d = 0, V = 0, chunk = 0;  // chunk = rows of the largest chunk (<= T)
+  int dtype = 0, mode = 0;
+  int64_t ldv = 0;      // row stride (elements) of the chunk logit/gradient buffer
+  int64_t ntiles = 0;   // row-statistics tiles per row = ceil(V / kStatW)
+  int splits = 1;       // dH split-K factor (tensor-core path)
+  size_t esize = 0;     // bytes per element of the chunk buffer
+  size_t off_zg = 0, off_part = 0, off_zy = 0, off_rowv = 0, off_dhp = 0;
+  size_t off_tokloss = 0, off_logp = 0, off_seqw = 0, off_scal = 0, off_cnt = 0;
+  int64_t n_chunks = 0, max_seq = 0;
+  size_t total = 0;
+};
+
+// Fills `L`; returns false for arguments no call can accept.
+bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L);
+
+// dH split-K factor of the tensor-core backward kernel for a chunk of `rows` rows.
+int choose_splits(int64_t rows, int64_t d, int64_t V, int num_sms);
+int num_sms();
+
+// ----- launchers (enqueue only; return cudaError_t of the launch) -----
+
+// tensor-core kernels (bf16 operands), sbp_tc.cu
+struct TcFwdArgs {
+  const void* H; const void* W; int64_t T, d, V;
+  int64_t r0; int rows;
+  const int32_t* labels;   // labels of the chunk (already offset by r0)
+  int32_t ignore_index;
+  void* E; int64_t lde;    // fp16 exp(z - tile max), [rows, lde]; nullptr: statistics only
+  float2* part; float* zy;
+  int32_t* status;
+};
+cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s);
+
+struct TcBwdArgs {
+  const void* G; int64_t ldg;   // bf16 [rows, ldg]
+  const void* H; const void* W; int64_t T, d, V;
+  int64_t r0; int rows;
+  int splits;
+  float* dh_part;               // [splits, rows, d] fp32
+  float* dW; int dw_accumulate;
+  uint32_t* counter;            // zero before launch
+  int32_t* status;
+};
+cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s);
+
+// SIMT fp32 kernels (fp32 operands), sbp_simt.cu
+cudaError_t simt_forward(const float* H, const float* W, int64_t d, int64_t V, int64_t r0, int rows,
+                         const int32_t* labels, int32_t ign, float* E, int64_t lde, float2* part,
+                         float* zy, bool store_e, cudaStream_t s);
+cudaError_t simt_backward(const float* G, int64_t ldg, const float* H, const float* W, int64_t d,
+                          int64_t V, int64_t r0, int rows, float* dh_part, float* dW,
+                          int dw_accumulate, cudaStream_t s);
+
+}  // namespace sbp

@@ -1,0 +1,702 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernels of the bf16 LM-head path, sm_103a.
+//
+// Both kernels are persistent, warp-specialised GEMMs with 128x256 fp32 accumulators in
+// tensor memory (two buffers, 512 columns) and a 4-stage TMA -> shared-memory ring:
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane issues tcgen05.mma)
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (one accumulator row per
+//               thread) and columns [128*h, 128*h+128) of the tile, h = (w-2)/4.
+//
+// k_fwd  : Z_c = H_c W^T  (A = H rows, B = W rows, both K-major), epilogue = row
+//          statistics per 128-column tile: max m, e = exp(z - m) stored as fp16,
+//          s = sum e, and the label logit z_y (the chunk forward of the StreamBP LM head).
+// k_bwd  : one dynamic queue of units of two kinds, dH first:
+//          dH_c = G_c W    (A = G rows, K-major; B = W, MN-major), split along V,
+//          dW  += G_c^T H_c (A = G columns, MN-major; B = H_c, MN-major).
+//
+// Every mbarrier wait is bounded in time: past the limit the kernel records
+// SBP_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded) for its own
+// copies and MMAs in flight, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "sbp_internal.h"
+
+namespace sbp {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t BOX_BYTES = 64 * 64 * 2; // one 64x64 bf16 box (MN-major operands)
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int RING = 4;
+constexpr float L2E = 1.4426950408889634f;
+
+struct Ctrl {
+  uint64_t full[STAGES], empty[STAGES];
+  uint64_t tfull[2], tempty[2];
+  uint64_t rfull[RING], rempty[RING];
+  uint64_t mdone;
+  int ring[RING];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), A / B major-ness (bit 15 / 16: 0 = K-major, 1 = MN-major),
+// N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t IDESC_FWD = idesc_bf16(BM, BN, false, false);
+constexpr uint32_t IDESC_DH = idesc_bf16(BM, BN, false, true);
+constexpr uint32_t IDESC_DW = idesc_bf16(BM, BN, true, true);
+
+// ------------------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(saddr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of parity `parity` of barrier b.  Returns false when the time
+// limit passes or (if abort_flag is given) another role of the CTA has aborted.
+__device__ __noinline__ bool wait_slow(uint64_t* b, uint32_t parity, const volatile int* abort_flag,
+                                       uint64_t limit_ns) {
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (gtimer() - t0 > limit_ns) return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_bounded(uint64_t* b, uint32_t parity, const volatile int* abort_flag,
+                                             uint64_t limit_ns) {
+  if (mbar_try(b, parity)) return true;
+  return wait_slow(b, parity, abort_flag, limit_ns);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1 (bit 46).
+// K-major tiles: rows of 128 B, 8-row groups 1024 B apart (SBO); LBO unused.
+// MN-major tiles: K rows of 128 B (64 MN elements), 8-row K groups 1024 B apart (SBO),
+// consecutive 64-element MN blocks LBO bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fail(Ctrl* c, int32_t* status) {
+  *(volatile int*)&c->abort = 1;
+  if (status) atomicCAS(status, 0, SBP_ERR_TIMEOUT);
+}
+
+// Warp-uniform bounded wait: all lanes poll, the warp proceeds only if every lane saw
+// the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, Ctrl* c, uint64_t limit) {
+  const bool ok = wait_bounded(b, parity, &c->abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Common prologue: barrier init, TMEM allocation (warp 1), and the hand-off of the
+// TMEM base address to all warps.
+__device__ __forceinline__ void prologue(Ctrl* c, int warp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&c->full[i], 1);
+      mbar_init(&c->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->tfull[i], 1);
+      mbar_init(&c->tempty[i], NUM_EPI_WARPS * 32);
+    }
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&c->rfull[i], 1);
+      mbar_init(&c->rempty[i], 1 + NUM_EPI_WARPS);
+    }
+    mbar_init(&c->mdone, 1);
+    c->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(&c->tmem_base, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+// Producer teardown after an abort: wait (bounded, ignoring the abort flag) until every
+// copy it issued has landed, so no TMA write is pending when the CTA exits.
+__device__ __forceinline__ void drain_copies(Ctrl* c, const uint32_t* last_phase, uint32_t issued_mask) {
+  for (int s = 0; s < STAGES; ++s)
+    if (issued_mask & (1u << s)) wait_bounded(&c->full[s], last_phase[s], nullptr, 200000000ull);
+}
+
+// MMA teardown: a final commit tracks every MMA this thread issued; wait for it.
+__device__ __forceinline__ void drain_mma(Ctrl* c) {
+  mma_commit(&c->mdone);
+  wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
+}
+
+__device__ __forceinline__ void epilogue_teardown(Ctrl* c, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(c->tmem_base, TMEM_COLS);
+  }
+}
+
+// ==================================================================================== forward
+
+struct FwdP {
+  int64_t r0; int rows; int64_t V;
+  int mt, ntn, kb;
+  const int32_t* labels;
+  __half* E; int64_t lde;
+  float2* part; int64_t ntiles; float* zy;
+  int32_t* status; uint64_t limit_ns;
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_fwd(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW, const FwdP p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  prologue(c, warp);
+  const uint32_t tmem = c->tmem_base;
+  const int total = p.mt * p.ntn;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_map(&tmH);
+      prefetch_map(&tmW);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0};
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int mb = tile % p.mt, nb = tile / p.mt;
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!wait_bounded(&c->empty[stage], phase ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
+          mbar_expect_tx(&c->full[stage], STAGE_BYTES);
+          tma_load_2d(sa, &tmH, &c->full[stage], kb * BK, (int)(p.r0 + (int64_t)mb * BM));
+          tma_load_2d(sb, &tmW, &c->full[stage], kb * BK, nb * BN);
+          issued |= 1u << stage;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        fail(c, p.status);
+        drain_copies(c, last_phase, issued);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!wait_bounded(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!wait_bounded(&c->full[stage], phase, &c->abort, p.limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), sw128_desc(sb + k * 32, 16, 1024), IDESC_FWD,
+                     (kb | k) != 0);
+          mma_commit(&c->empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&c->tfull[buf]);
+      }
+      if (!ok) fail(c, p.status);
+      drain_mma(c);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int lrow = q * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const int mb = tile % p.mt, nb = tile / p.mt;
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      const int row = mb * BM + lrow;
+      const bool vrow = row < p.rows;
+      const int32_t y = vrow ? p.labels[row] : INT_MIN;
+      if (!warp_wait(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
+        fail(c, p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
+      const int64_t c0 = (int64_t)nb * BN + h * 128;
+      float m = -INFINITY, zyv = 0.f;
+      bool has_y = false;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tb + g * 32, r);
+        tmem_ld_wait();
+        const int64_t cg = c0 + g * 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float v = __uint_as_float(r[j]);
+          if (cg + j < p.V) m = fmaxf(m, v);
+          if (cg + j == (int64_t)y) { zyv = v; has_y = true; }
+        }
+      }
+      const float mb2 = m * L2E;
+      float s = 0.f;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tb + g * 32, r);
+        tmem_ld_wait();
+        const int64_t cg = c0 + g * 32;
+        if (cg >= p.V) continue;
+        uint32_t hv[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float e0 = (cg + j < p.V) ? ex2(fmaf(__uint_as_float(r[j]), L2E, -mb2)) : 0.f;
+          const float e1 = (cg + j + 1 < p.V) ? ex2(fmaf(__uint_as_float(r[j + 1]), L2E, -mb2)) : 0.f;
+          s += e0 + e1;
+          const __half2 hh = __floats2half2_rn(e0, e1);
+          hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        if (p.E && vrow) {
+          uint4* dst = reinterpret_cast<uint4*>(p.E + (int64_t)row * p.lde + cg);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&c->tempty[buf]);
+      const int64_t tix = (int64_t)nb * 2 + h;
+      if (vrow && tix < p.ntiles) p.part[(int64_t)row * p.ntiles + tix] = make_float2(m, s);
+      if (vrow && has_y) p.zy[row] = zyv;
+    }
+  }
+  epilogue_teardown(c, warp);
+}
+
+// =================================================================================== backward
+
+struct BwdP {
+  int rows; int64_t r0; int64_t V, d;
+  int mt_c, nt_d, kb_v, splits, mt_v, kb_c;
+  int n_dh, n_total;
+  float* dh_part; int64_t plane;
+  float* dW; int dw_acc;
+  uint32_t* counter;
+  int32_t* status; uint64_t limit_ns;
+};
+
+struct Unit {
+  int kind;   // 0 = dH, 1 = dW
+  int mb, nb, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode(const BwdP& p, int u) {
+  Unit w;
+  if (u < p.n_dh) {
+    w.kind = 0;
+    w.mb = u % p.mt_c;
+    w.nb = (u / p.mt_c) % p.nt_d;
+    w.split = u / (p.mt_c * p.nt_d);
+    w.kb0 = (int)((int64_t)w.split * p.kb_v / p.splits);
+    w.kb1 = (int)((int64_t)(w.split + 1) * p.kb_v / p.splits);
+  } else {
+    u -= p.n_dh;
+    w.kind = 1;
+    w.nb = u % p.nt_d;
+    w.mb = u / p.nt_d;
+    w.split = 0;
+    w.kb0 = 0;
+    w.kb1 = p.kb_c;
+  }
+  return w;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_bwd(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmGmn,
+          const __grid_constant__ CUtensorMap tmWmn, const __grid_constant__ CUtensorMap tmHmn, const BwdP p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  prologue(c, warp);
+  const uint32_t tmem = c->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_map(&tmGk);
+      prefetch_map(&tmGmn);
+      prefetch_map(&tmWmn);
+      prefetch_map(&tmHmn);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0};
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int slot = i % RING;
+        const uint32_t rph = (uint32_t)((i / RING) & 1);
+        if (!wait_bounded(&c->rempty[slot], rph ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        int u = (int)atomicAdd(p.counter, 1u);
+        if (u >= p.n_total) u = -1;
+        c->ring[slot] = u;
+        mbar_arrive(&c->rfull[slot]);
+        if (u < 0) break;
+        const Unit w = decode(p, u);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!wait_bounded(&c->empty[stage], phase ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
+          uint64_t* fb = &c->full[stage];
+          mbar_expect_tx(fb, STAGE_BYTES);
+          if (w.kind == 0) {
+            tma_load_2d(sa, &tmGk, fb, kb * BK, w.mb * BM);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmWmn, fb, w.nb * BN + j * 64, kb * BK);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * BOX_BYTES, &tmGmn, fb, w.mb * BM + j * 64, kb * BK);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sb + j * BOX_BYTES, &tmHmn, fb, w.nb * BN + j * 64, (int)(p.r0 + (int64_t)kb * BK));
+          }
+          issued |= 1u << stage;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        fail(c, p.status);
+        drain_copies(c, last_phase, issued);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int i = 0; ok; ++i, ++local) {
+        const int slot = i % RING;
+        const uint32_t rph = (uint32_t)((i / RING) & 1);
+        if (!wait_bounded(&c->rfull[slot], rph, &c->abort, p.limit_ns)) { ok = false; break; }
+        const int u = c->ring[slot];
+        mbar_arrive(&c->rempty[slot]);
+        if (u < 0) break;
+        const Unit w = decode(p, u);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!wait_bounded(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(buf * BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!wait_bounded(&c->full[stage], phase, &c->abort, p.limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
+          const uint32_t acc0 = kb != w.kb0 ? 1u : 0u;
+          if (w.kind == 0) {
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), sw128_desc(sb + k * 2048, BOX_BYTES, 1024), IDESC_DH,
+                       acc0 | (k != 0));
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16(dt, sw128_desc(sa + k * 2048, BOX_BYTES, 1024), sw128_desc(sb + k * 2048, BOX_BYTES, 1024),
+                       IDESC_DW, acc0 | (k != 0));
+          }
+          mma_commit(&c->empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&c->tfull[buf]);
+      }
+      if (!ok) fail(c, p.status);
+      drain_mma(c);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int lrow = q * 32 + lane;
+    int local = 0;
+    for (int i = 0;; ++i, ++local) {
+      const int slot = i % RING;
+      const uint32_t rph = (uint32_t)((i / RING) & 1);
+      if (!warp_wait(&c->rfull[slot], rph, c, p.limit_ns)) {
+        fail(c, p.status);
+        break;
+      }
+      const int u = c->ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->rempty[slot]);
+      if (u < 0) break;
+      const Unit w = decode(p, u);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!warp_wait(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
+        fail(c, p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
+      const int64_t c0 = (int64_t)w.nb * BN + h * 128;
+      const int64_t row = (int64_t)w.mb * BM + lrow;
+      float* dst;
+      bool vrow;
+      if (w.kind == 0) {
+        vrow = row < p.rows;
+        dst = p.dh_part + (int64_t)w.split * p.plane + row * p.d;
+      } else {
+        vrow = row < p.V;
+        dst = p.dW + row * p.d;
+      }
+      const bool add = w.kind == 1 && p.dw_acc;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tb + g * 32, r);
+        tmem_ld_wait();
+        const int64_t cg = c0 + g * 32;
+        if (!vrow || cg >= p.d) continue;
+        float* o = dst + cg;
+        if (cg + 32 <= p.d) {
+          float4* o4 = reinterpret_cast<float4*>(o);
+          if (add) {
+            float4 old[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) old[k] = o4[k];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o4[k] = make_float4(old[k].x + __uint_as_float(r[4 * k]), old[k].y + __uint_as_float(r[4 * k + 1]),
+                                  old[k].z + __uint_as_float(r[4 * k + 2]), old[k].w + __uint_as_float(r[4 * k + 3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o4[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                  __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (cg + j < p.d) o[j] = add ? o[j] + __uint_as_float(r[j]) : __uint_as_float(r[j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&c->tempty[buf]);
+    }
+  }
+  epilogue_teardown(c, warp);
+}
+
+// ======================================================================================= host
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] array with a row stride of
+// row_elems elements, 128-byte swizzle, zero fill outside the array.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_elems, uint32_t box_in,
+              uint32_t box_out) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {box_in, box_out};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* e = std::getenv("SBP_WAIT_LIMIT_MS");
+    long long ms = e ? std::atoll(e) : 0;
+    if (ms <= 0) ms = 2000;
+    return (uint64_t)ms * 1000000ull;
+  }();
+  return v;
+}
+
+bool set_smem_attr() {
+  static int done = 0;  // 1 ok, -1 failed
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done == 0) {
+    const bool ok = cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) ==
+                        cudaSuccess &&
+                    cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) ==
+                        cudaSuccess;
+    done = ok ? 1 : -1;
+  }
+  return done == 1;
+}
+
+}  // namespace tc
+
+cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
+  using namespace tc;
+  if (!set_smem_attr()) return cudaErrorInvalidConfiguration;
+  CUtensorMap mH, mW;
+  if (!make_map(&mH, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mW, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, BK, BN)) return cudaErrorInvalidValue;
+  FwdP p;
+  p.r0 = a.r0; p.rows = a.rows; p.V = a.V;
+  p.mt = (a.rows + BM - 1) / BM;
+  p.ntn = (int)((a.V + BN - 1) / BN);
+  p.kb = (int)((a.d + BK - 1) / BK);
+  p.labels = a.labels;
+  p.E = static_cast<__half*>(a.E); p.lde = a.lde;
+  p.part = a.part; p.ntiles = (a.V + kStatW - 1) / kStatW; p.zy = a.zy;
+  p.status = a.status; p.limit_ns = wait_limit_ns();
+  const int total = p.mt * p.ntn;
+  int grid = num_sms();
+  if (grid > total) grid = total;
+  k_fwd<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mH, mW, p);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
+  using namespace tc;
+  if (!set_smem_attr()) return cudaErrorInvalidConfiguration;
+  CUtensorMap mGk, mGmn, mWmn, mHmn;
+  // G: [rows, V] with row stride ldg; rows past the chunk read as zero.
+  if (!make_map(&mGk, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mGmn, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&mWmn, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&mHmn, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  BwdP p;
+  p.rows = a.rows; p.r0 = a.r0; p.V = a.V; p.d = a.d;
+  p.mt_c = (a.rows + BM - 1) / BM;
+  p.nt_d = (int)((a.d + BN - 1) / BN);
+  p.kb_v = (int)((a.V + BK - 1) / BK);
+  p.splits = a.splits;
+  p.mt_v = (int)((a.V + BM - 1) / BM);
+  p.kb_c = (a.rows + BK - 1) / BK;
+  p.n_dh = p.mt_c * p.nt_d * p.splits;
+  p.n_total = p.n_dh + p.mt_v * p.nt_d;
+  p.dh_part = a.dh_part; p.plane = (int64_t)a.rows * a.d;
+  p.dW = a.dW; p.dw_acc = a.dw_accumulate;
+  p.counter = a.counter; p.status = a.status; p.limit_ns = wait_limit_ns();
+  int grid = num_sms();
+  if (grid > p.n_total) grid = p.n_total;
+  k_bwd<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mGk, mGmn, mWmn, mHmn, p);
+  return cudaGetLastError();
+}
+
+}  // namespace sbp

@@ -54,12 +54,13 @@ def _normal(seed: int, what: str, shape, std: float, bf16: bool, block_rows: int
     return out
 
 
-def make_hw(T: int, d: int, V: int, seed: int, dtype: str):
-    """H [T, d] and W [V, d] as float32 arrays holding values exact in ``dtype``."""
+def make_hw(T: int, d: int, V: int, seed: int, dtype: str, w_std: float = 0.02):
+    """H [T, d] ~ N(0, 1) and W [V, d] ~ N(0, w_std^2) as float32 arrays holding values
+    exact in ``dtype``."""
     if dtype not in ("bf16", "fp32"):
         raise ValueError(dtype)
     H = _normal(seed, "H", (T, d), 1.0, dtype == "bf16")
-    W = _normal(seed, "W", (V, d), 0.02, dtype == "bf16")
+    W = _normal(seed, "W", (V, d), w_std, dtype == "bf16")
     return H, W
 
 

@@ -1,0 +1,235 @@
+"""Python binding of libsbp.so (argument marshalling only).
+
+Every function here checks shapes, takes raw device pointers from PyTorch tensors,
+and calls the C entry point of the same name (see ``include/sbp.h``).  All
+arithmetic runs in the library's CUDA kernels; PyTorch only provides device memory
+and the current stream.  Importing this module loads the library and raises if it
+has not been built (``__graft_entry__.build()``) -- there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsbp.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "sbp.h")
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_LABEL_RANGE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED = range(8)
+BF16, FP32 = 0, 1
+MODE_SFT, MODE_GRPO, MODE_DPO1, MODE_DPO2 = 0, 1, 2, 3
+IGNORE_INDEX = -100
+
+
+class SbpError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                          "(the LM-head kernels have no other implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I32, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    C = ctypes.c_int
+    lib.sbp_lmhead_workspace_bytes.restype = SZ
+    lib.sbp_lmhead_workspace_bytes.argtypes = [I64, I64, I64, I64, C, C]
+    lib.sbp_lmhead_sft.restype = C
+    lib.sbp_lmhead_sft.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, SZ, P, P]
+    lib.sbp_lmhead_grpo.restype = C
+    lib.sbp_lmhead_grpo.argtypes = [P, P, P, P, P, F, F, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, SZ, P, P]
+    lib.sbp_lmhead_dpo_pass1.restype = C
+    lib.sbp_lmhead_dpo_pass1.argtypes = [P, P, P, P, I32, I64, I64, I64, I64, I32, C, P, P, P, P, SZ, P, P]
+    lib.sbp_lmhead_dpo_pass2.restype = C
+    lib.sbp_lmhead_dpo_pass2.argtypes = [P, P, P, P, I32, P, P, F, I64, I64, I64, I64, I32, C, P, P, P, P, C, P,
+                                         SZ, P, P]
+    lib.sbp_status_string.restype = ctypes.c_char_p
+    lib.sbp_status_string.argtypes = [C]
+    lib.sbp_last_launch_count.restype = C
+    lib.sbp_last_launch_count.argtypes = []
+    lib.sbp_profile_enable.restype = C
+    lib.sbp_profile_enable.argtypes = [C]
+    lib.sbp_profile_read.restype = C
+    lib.sbp_profile_read.argtypes = [P, P, C]
+    return lib
+
+
+_lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/sbp.h`` declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sbp_[a-z0-9_]+)\s*\(", src)))
+
+
+def status_string(code: int) -> str:
+    return _lib.sbp_status_string(int(code)).decode()
+
+
+def last_launch_count() -> int:
+    return int(_lib.sbp_last_launch_count())
+
+
+KERNEL_CLASSES = ("forward_gemm", "backward_gemm", "logit_grad", "other")
+
+
+def profile_enable(on: bool = True) -> None:
+    _lib.sbp_profile_enable(1 if on else 0)
+
+
+def profile_read() -> dict:
+    """Per kernel class: (total ms, launches) recorded since the last read."""
+    n = len(KERNEL_CLASSES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    r = _lib.sbp_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p), n)
+    if r < 0:
+        raise SbpError(-r, "sbp_profile_read")
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+def workspace_bytes(T: int, d: int, V: int, chunk: int, dtype: int, mode: int) -> int:
+    return int(_lib.sbp_lmhead_workspace_bytes(T, d, V, chunk, dtype, mode))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise SbpError(code, where)
+
+
+def make_workspace(T, d, V, chunk, dtype, mode, device=None) -> torch.Tensor:
+    n = workspace_bytes(T, d, V, chunk, dtype, mode)
+    if n == 0:
+        raise SbpError(ERR_INVALID_ARG, "workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _prep(H, W, labels, chunk, mode, workspace):
+    _dev(H, W, labels)
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    T, d = H.shape
+    V = W.shape[0]
+    if W.shape[1] != d or H.dtype != W.dtype or labels.shape != (T,):
+        raise ValueError("shape/dtype mismatch between H [T,d], W [V,d], labels [T]")
+    dt = _code(H)
+    if workspace is None:
+        workspace = make_workspace(T, d, V, chunk, dt, mode, H.device)
+    return T, d, V, dt, workspace
+
+
+def _grad_out(H, W, dH, dW):
+    if dH is None:
+        dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty(W.shape, dtype=torch.float32, device=W.device)
+    _dev(dH, dW)
+    return dH, dW
+
+
+def sft(H, W, labels, chunk, ignore_index=IGNORE_INDEX, *, dH=None, dW=None, accumulate_dW=False,
+        logp=True, workspace=None, status=None, stream=None) -> dict:
+    """SFT cross-entropy forward + backward (``sbp_lmhead_sft``).  Returns device tensors."""
+    T, d, V, dt, ws = _prep(H, W, labels, chunk, MODE_SFT, workspace)
+    dH, dW = _grad_out(H, W, dH, dW)
+    dev = H.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    nv = torch.empty((), dtype=torch.int64, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev) if logp else None
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_lmhead_sft(_p(H), _p(W), _p(labels), T, d, V, chunk, ignore_index, dt, _p(loss), _p(nv),
+                               _p(lp), _p(dH), _p(dW), int(bool(accumulate_dW)), _p(ws), ws.numel(), _p(st),
+                               _stream(stream)), "sbp_lmhead_sft")
+    return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
+
+
+def grpo(H, W, labels, advantages, logp_old, chunk, clip_lo=0.8, clip_hi=1.2, ignore_index=IGNORE_INDEX, *,
+         dH=None, dW=None, accumulate_dW=False, logp=True, workspace=None, status=None, stream=None) -> dict:
+    """GRPO / PPO-clip forward + backward (``sbp_lmhead_grpo``)."""
+    T, d, V, dt, ws = _prep(H, W, labels, chunk, MODE_GRPO, workspace)
+    _dev(advantages, logp_old)
+    if advantages.dtype != torch.float32 or logp_old.dtype != torch.float32:
+        raise TypeError("advantages and logp_old must be float32")
+    dH, dW = _grad_out(H, W, dH, dW)
+    dev = H.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    nv = torch.empty((), dtype=torch.int64, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev) if logp else None
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_lmhead_grpo(_p(H), _p(W), _p(labels), _p(advantages), _p(logp_old), clip_lo, clip_hi, T, d, V,
+                                chunk, ignore_index, dt, _p(loss), _p(nv), _p(lp), _p(dH), _p(dW),
+                                int(bool(accumulate_dW)), _p(ws), ws.numel(), _p(st), _stream(stream)),
+           "sbp_lmhead_grpo")
+    return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
+
+
+def dpo_pass1(H, W, labels, cu_seqlens, chunk, ignore_index=IGNORE_INDEX, *, logp=True, workspace=None,
+              status=None, stream=None) -> dict:
+    """DPO first pass: per-sequence summed label log-probs (``sbp_lmhead_dpo_pass1``)."""
+    T, d, V, dt, ws = _prep(H, W, labels, chunk, MODE_DPO1, workspace)
+    _dev(cu_seqlens)
+    n_seq = cu_seqlens.numel() - 1
+    dev = H.device
+    S = torch.empty(max(n_seq, 0), dtype=torch.float64, device=dev)
+    nv = torch.empty((), dtype=torch.int64, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev) if logp else None
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_lmhead_dpo_pass1(_p(H), _p(W), _p(labels), _p(cu_seqlens), n_seq, T, d, V, chunk,
+                                     ignore_index, dt, _p(S), _p(lp), _p(nv), _p(ws), ws.numel(), _p(st),
+                                     _stream(stream)), "sbp_lmhead_dpo_pass1")
+    return dict(seq_logp=S, logp=lp, n_valid=nv, status=st)
+
+
+def dpo_pass2(H, W, labels, cu_seqlens, seq_logp, ref_seq_logp, beta, chunk, ignore_index=IGNORE_INDEX, *,
+              dH=None, dW=None, accumulate_dW=False, workspace=None, status=None, stream=None) -> dict:
+    """DPO second pass: loss and gradients given the sequence sums (``sbp_lmhead_dpo_pass2``)."""
+    T, d, V, dt, ws = _prep(H, W, labels, chunk, MODE_DPO2, workspace)
+    _dev(cu_seqlens, seq_logp, ref_seq_logp)
+    n_seq = cu_seqlens.numel() - 1
+    dH, dW = _grad_out(H, W, dH, dW)
+    dev = H.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    margins = torch.empty(max(n_seq // 2, 1), dtype=torch.float64, device=dev)
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_lmhead_dpo_pass2(_p(H), _p(W), _p(labels), _p(cu_seqlens), n_seq, _p(seq_logp),
+                                     _p(ref_seq_logp), float(beta), T, d, V, chunk, ignore_index, dt, _p(loss),
+                                     _p(margins), _p(dH), _p(dW), int(bool(accumulate_dW)), _p(ws), ws.numel(),
+                                     _p(st), _stream(stream)), "sbp_lmhead_dpo_pass2")
+    return dict(loss=loss, margins=margins[: n_seq // 2], dH=dH, dW=dW, status=st)
+
+
+def check_status(status: torch.Tensor, where: str = "device") -> None:
+    """Raise if a call's device status word (read after synchronising) is not SBP_OK."""
+    code = int(status.item())
+    if code != OK:
+        raise SbpError(code, where)

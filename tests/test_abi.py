@@ -1,0 +1,105 @@
+"""Host-side checks of the C-ABI library (CPU only: no kernel is launched).
+
+The library must build, load and export every function ``include/sbp.h`` declares;
+the workspace query and the argument checks (which run on the host before anything
+is enqueued) must behave as the header states.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sbp():
+    from memory_efficient_exact_gb300 import _build
+    _build.build_library()
+    from memory_efficient_exact_gb300 import sbp as mod
+    return mod
+
+
+def test_library_exports_every_header_function(sbp):
+    names = sbp.header_functions()
+    assert {"sbp_lmhead_sft", "sbp_lmhead_grpo", "sbp_lmhead_dpo_pass1", "sbp_lmhead_dpo_pass2",
+            "sbp_lmhead_workspace_bytes"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", sbp.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(sbp.LIB_PATH)
+    for n in names:
+        getattr(lib, n)
+
+
+def test_status_strings(sbp):
+    assert sbp.status_string(0) == "SBP_OK"
+    assert sbp.status_string(4) == "SBP_ERR_LABEL_RANGE"
+    assert sbp.status_string(99) == "SBP_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(sbp):
+    V, d = 151936, 4096
+    w1 = sbp.workspace_bytes(16384, d, V, 2048, sbp.BF16, sbp.MODE_SFT)
+    w2 = sbp.workspace_bytes(65536, d, V, 2048, sbp.BF16, sbp.MODE_SFT)
+    assert w1 > 2048 * V * 2                       # at least one chunk of logits (fp16/bf16)
+    assert w1 < 2048 * V * 2 * 2                   # ... and far below two
+    assert w2 - w1 < 64 * 65536                    # T enters only through O(T) scalars
+    assert sbp.workspace_bytes(16384, d, V, 4096, sbp.BF16, sbp.MODE_SFT) > w1
+    # fp32 path keeps fp32 logits
+    assert sbp.workspace_bytes(256, 64, 1000, 64, sbp.FP32, sbp.MODE_SFT) >= 64 * 1000 * 4
+    # invalid arguments
+    assert sbp.workspace_bytes(16, 0, 10, 4, sbp.BF16, 0) == 0
+    assert sbp.workspace_bytes(16, 8, 10, 0, sbp.BF16, 0) == 0
+    assert sbp.workspace_bytes(16, 8, 10, 4, 7, 0) == 0
+    assert sbp.workspace_bytes(16, 8, 10, 4, sbp.BF16, 9) == 0
+    # the chunk never exceeds T
+    assert sbp.workspace_bytes(10, 64, 1000, 4096, sbp.FP32, 0) == sbp.workspace_bytes(10, 64, 1000, 10, sbp.FP32, 0)
+
+
+def _call_sft(lib, **kw):
+    a = dict(H=0x1000, W=0x2000, labels=0x3000, T=16, d=64, V=128, chunk=8, ign=-100, dtype=0, loss=0x4000,
+             nv=0x5000, lp=None, dH=0x6000, dW=0x7000, acc=0, ws=0x100000, wsb=1 << 30, st=0x8000, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.sbp_lmhead_sft(P(a["H"]), P(a["W"]), P(a["labels"]), a["T"], a["d"], a["V"], a["chunk"], a["ign"],
+                              a["dtype"], P(a["loss"]), P(a["nv"]), P(a["lp"]), P(a["dH"]), P(a["dW"]), a["acc"],
+                              P(a["ws"]), a["wsb"], P(a["st"]), P(a["stream"]))
+
+
+def test_argument_errors_are_caught_on_the_host(sbp):
+    # Every case below fails validation before any CUDA call, so the fake device
+    # addresses are never touched.
+    lib = sbp._lib
+    assert _call_sft(lib, W=None) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, st=None) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, dW=None) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, loss=None) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, d=-1) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, chunk=0) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, dtype=5) == sbp.ERR_INVALID_ARG
+    assert _call_sft(lib, d=60) == sbp.ERR_UNSUPPORTED        # bf16 rows must be 16-byte multiples
+    assert _call_sft(lib, V=100) == sbp.ERR_UNSUPPORTED
+    assert _call_sft(lib, H=0x1008) == sbp.ERR_ALIGNMENT
+    assert _call_sft(lib, ws=0x100010) == sbp.ERR_WORKSPACE    # not 256-byte aligned
+    assert _call_sft(lib, wsb=16) == sbp.ERR_WORKSPACE          # too small
+    P = ctypes.c_void_p
+    # GRPO without advantages, DPO pass 2 with an odd number of sequences
+    r = lib.sbp_lmhead_grpo(P(0x1000), P(0x2000), P(0x3000), None, P(0x9000), 0.8, 1.2, 16, 64, 128, 8, -100, 0,
+                            P(0x4000), None, None, P(0x6000), P(0x7000), 0, P(0x100000), 1 << 30, P(0x8000), None)
+    assert r == sbp.ERR_INVALID_ARG
+    r = lib.sbp_lmhead_dpo_pass2(P(0x1000), P(0x2000), P(0x3000), P(0x9000), 3, P(0xa000), P(0xb000), 0.1,
+                                 16, 64, 128, 8, -100, 0, P(0x4000), None, P(0x6000), P(0x7000), 0,
+                                 P(0x100000), 1 << 30, P(0x8000), None)
+    assert r == sbp.ERR_INVALID_ARG
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "memory_efficient_exact_gb300")
+    for dp, _, fs in os.walk(pkg):
+        for f in fs:
+            if f.endswith((".py", ".cu", ".h", ".cuh")):
+                src = open(os.path.join(dp, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f

@@ -1,0 +1,182 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small and medium shapes that the oracle finishes in seconds but that still span
+several 128x256 tiles, several chunks and ragged tails in T, d, V and the chunk;
+every objective; the edge cases (empty batch, all tokens ignored, a chunk larger
+than T, chunk = 1, accumulation into dW, labels out of range) and determinism.
+"""
+import numpy as np
+import pytest
+
+from oracle import lmhead as O
+from memory_efficient_exact_gb300 import inputs as I
+from parity_util import TOL, rel, rel_fro, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+IGN = -100
+
+
+@pytest.fixture(scope="module")
+def sbp():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from memory_efficient_exact_gb300 import _build
+    _build.build_library()
+    from memory_efficient_exact_gb300 import sbp as mod
+    return mod
+
+
+def make_case(T, d, V, dtype, seed, w_std=0.02, frac=0.1):
+    H, W = I.make_hw(T, d, V, seed, dtype, w_std=w_std)
+    y = I.make_labels(T, V, seed, "frac", frac)
+    return H, W, y
+
+
+def check_grads(dtype, out, ref, y):
+    tol = TOL[dtype]
+    dH = out["dH"].float().cpu().numpy()
+    dW = out["dW"].cpu().numpy()
+    assert rel_fro(dH, ref["dH"]) <= tol["grad"], rel_fro(dH, ref["dH"])
+    assert rel_fro(dW, ref["dW"]) <= tol["grad"], rel_fro(dW, ref["dW"])
+    ign = np.asarray(y) == IGN
+    assert np.all(dH[ign] == 0.0), "rows of ignored tokens must be exactly zero"
+    return dH, dW
+
+
+SFT_CASES = [
+    # dtype, T, d, V, chunk, w_std
+    ("fp32", 256, 64, 1000, 64, 0.02),      # the fp32 workload of the spec
+    ("fp32", 77, 36, 531, 16, 0.3),          # ragged everything
+    ("fp32", 40, 16, 97, 1, 0.5),            # chunk = 1
+    ("bf16", 300, 256, 2000, 128, 0.05),    # several chunks, ragged last chunk and V tail
+    ("bf16", 517, 192, 1304, 200, 0.08),    # d < one 256-wide N tile; V not a tile multiple
+    ("bf16", 130, 72, 264, 64, 0.2),        # K tail (72 = 64 + 8)
+    ("bf16", 1000, 512, 4096, 384, 0.04),   # many tiles in every dimension
+    ("bf16", 640, 1024, 8200, 640, 0.03),   # d spans 4 N tiles, V spans 33 (tail of 8)
+]
+
+
+@pytest.mark.parametrize("dtype,T,d,V,chunk,w_std", SFT_CASES)
+def test_sft_parity(sbp, dtype, T, d, V, chunk, w_std):
+    H, W, y = make_case(T, d, V, dtype, seed=11 + T, w_std=w_std)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    out = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.sft(H, W, y, IGN)
+    tol = TOL[dtype]
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= tol["loss"], (out["loss"].item(), ref["loss"])
+    lp = out["logp"].cpu().numpy()
+    assert np.max(np.abs(lp - ref["logp"])) <= tol["logp"] * max(1.0, np.abs(ref["logp"]).max())
+    assert np.all(lp[np.asarray(y) == IGN] == 0.0)
+    check_grads(dtype, out, ref, y)
+
+
+@pytest.mark.parametrize("dtype,T,d,V,chunk", [("fp32", 64, 32, 200, 16), ("bf16", 300, 256, 2000, 128),
+                                                ("bf16", 520, 128, 1000, 256)])
+def test_grpo_parity(sbp, dtype, T, d, V, chunk):
+    H, W, y = make_case(T, d, V, dtype, seed=7 + T, w_std=0.1)
+    f = O.forward(H, W, y, IGN)
+    n_resp = 4
+    L = (T + n_resp - 1) // n_resp
+    A = I.make_advantages(n_resp, L, seed=T)[:T].astype(np.float32)
+    lpo = (f["logp"] + I.make_logp_noise(T, seed=T)).astype(np.float32)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    out = sbp.grpo(Ht, Wt, yt, torch.from_numpy(A).cuda(), torch.from_numpy(lpo).cuda(), chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.grpo(H, W, y, A.astype(np.float64), lpo.astype(np.float64), IGN)
+    tol = TOL[dtype]
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= tol["loss"]
+    check_grads(dtype, out, ref, y)
+
+
+@pytest.mark.parametrize("dtype,lens,d,V,chunk", [("fp32", [30, 20, 25, 21], 32, 200, 40),
+                                                   ("bf16", [200, 96, 150, 74], 256, 2000, 128),
+                                                   ("bf16", [128, 256, 64, 192, 100, 100], 128, 1024, 100)])
+def test_dpo_parity(sbp, dtype, lens, d, V, chunk):
+    T = sum(lens)
+    H, W = I.make_hw(T, d, V, 99 + T, dtype, w_std=0.1)
+    y = I.make_labels(T, V, 99 + T, "frac", 0.2)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    n = len(lens)
+    f = O.dpo_pass1(H, W, y, cu, IGN)
+    # references close to the policy's own sums so that the margins spread around 0
+    ref_S = f["seq_logp"] + np.linspace(-3, 3, n)
+    beta = 0.5
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    cut = torch.from_numpy(cu).cuda()
+    p1 = sbp.dpo_pass1(Ht, Wt, yt, cut, chunk)
+    p2 = sbp.dpo_pass2(Ht, Wt, yt, cut, p1["seq_logp"], torch.from_numpy(ref_S).cuda(), beta, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(p1["status"])
+    sbp.check_status(p2["status"])
+    tol = TOL[dtype]
+    S = p1["seq_logp"].cpu().numpy()
+    assert np.max(np.abs(S - f["seq_logp"]) / np.abs(f["seq_logp"])) <= tol["seq"]
+    assert int(p1["n_valid"].item()) == f["n_valid"]
+    ref = O.dpo(H, W, y, cu, ref_S, beta, IGN)
+    assert rel(p2["loss"].item(), ref["loss"]) <= tol["loss"]
+    np.testing.assert_allclose(p2["margins"].cpu().numpy(), ref["margins"], rtol=0, atol=50 * tol["seq"])
+    check_grads(dtype, p2, ref, y)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_accumulate_dw_and_determinism(sbp, dtype):
+    T, d, V, chunk = 200, 128, 1000, 64
+    H, W, y = make_case(T, d, V, dtype, seed=5, w_std=0.1)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    a = sbp.sft(Ht, Wt, yt, chunk)
+    b = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(a["dH"], b["dH"]) and torch.equal(a["dW"], b["dW"]) and torch.equal(a["loss"], b["loss"])
+    acc = a["dW"].clone()
+    sbp.sft(Ht, Wt, yt, chunk, dW=acc, accumulate_dW=True)
+    torch.cuda.synchronize()
+    assert torch.allclose(acc, 2 * a["dW"], rtol=1e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_edge_cases(sbp, dtype):
+    d, V = 64, 512
+    # all tokens ignored -> loss 0, zero gradients, N = 0
+    H, W, y = make_case(50, d, V, dtype, seed=3)
+    y[:] = IGN
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    o = sbp.sft(Ht, Wt, yt, 16)
+    torch.cuda.synchronize()
+    assert o["loss"].item() == 0.0 and int(o["n_valid"].item()) == 0
+    assert torch.count_nonzero(o["dH"]).item() == 0 and torch.count_nonzero(o["dW"]).item() == 0
+    # empty batch: dW overwritten with zeros, loss 0
+    He = torch.empty((0, d), dtype=Ht.dtype, device="cuda")
+    ye = torch.empty((0,), dtype=torch.int32, device="cuda")
+    dW = torch.full((V, d), 7.0, device="cuda")
+    o = sbp.sft(He, Wt, ye, 16, dW=dW)
+    torch.cuda.synchronize()
+    assert o["loss"].item() == 0.0 and torch.count_nonzero(dW).item() == 0
+    # a chunk larger than T equals one chunk
+    H, W, y = make_case(50, d, V, dtype, seed=4, w_std=0.2)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    o1 = sbp.sft(Ht, Wt, yt, 4096)
+    o2 = sbp.sft(Ht, Wt, yt, 50)
+    torch.cuda.synchronize()
+    assert torch.equal(o1["dH"], o2["dH"]) and torch.equal(o1["dW"], o2["dW"])
+    ref = O.sft(H, W, y, IGN)
+    check_grads(dtype, o1, ref, y)
+
+
+def test_label_out_of_range_sets_device_status(sbp):
+    H, W, y = make_case(40, 64, 256, "bf16", seed=8)
+    y[5] = 256
+    Ht, Wt, yt = to_dev(torch, H, W, y, "bf16")
+    o = sbp.sft(Ht, Wt, yt, 16)
+    torch.cuda.synchronize()
+    assert int(o["status"].item()) == sbp.ERR_LABEL_RANGE
+    y[5] = -7
+    Ht, Wt, yt = to_dev(torch, H, W, y, "fp32")
+    o = sbp.sft(Ht, Wt, yt, 16)
+    torch.cuda.synchronize()
+    assert int(o["status"].item()) == sbp.ERR_LABEL_RANGE
