@@ -1,0 +1,175 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration of the bench.
+
+The oracle cannot materialise T x V float64 logits at these sizes, so it evaluates
+the same definitions row by row: every row's lse / logp (all rows: the loss and the
+DPO sums need them), dH on seeded sampled rows, dW on seeded sampled vocabulary rows
+(which needs every row's lse).  The 65536-token workload follows its own recipe:
+per-token loss and dH on sampled rows of the full run, and the full dW of the
+4096-token prefix sub-problem.
+"""
+import numpy as np
+import pytest
+
+from oracle import lmhead as O
+from memory_efficient_exact_gb300 import inputs as I
+from parity_util import TOL, rel, rel_fro
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+IGN = -100
+BF = TOL["bf16"]
+
+
+@pytest.fixture(scope="module")
+def sbp():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from memory_efficient_exact_gb300 import _build
+    _build.build_library()
+    from memory_efficient_exact_gb300 import sbp as mod
+    return mod
+
+
+def dev_inputs(H, W, y):
+    return (torch.from_numpy(H).cuda().to(torch.bfloat16), torch.from_numpy(W).cuda().to(torch.bfloat16),
+            torch.from_numpy(y).cuda())
+
+
+def vocab_sample(y, V, seed, k=48):
+    g = np.random.default_rng(seed)
+    lab = np.unique(y[y != IGN])
+    pick = np.concatenate([g.choice(lab, size=min(k // 2, len(lab)), replace=False), g.choice(V, size=k // 2)])
+    return np.unique(pick)
+
+
+def check_sampled(H, W, y, w, lse, out, rows, vocab, extra=""):
+    dH = out["dH"]
+    ign = torch.from_numpy(y == IGN).cuda()
+    assert torch.count_nonzero(dH[ign]).item() == 0, "ignored rows of dH must be exactly zero"
+    ref_dh = O.rows_dH(H, W, y, w, rows, IGN)
+    got_dh = dH[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    e = rel_fro(got_dh, ref_dh)
+    assert e <= BF["grad"], f"dH sampled rows {e}{extra}"
+    ref_dw = O.cols_dW(H, W, y, w, lse, vocab, IGN)
+    got_dw = out["dW"][torch.from_numpy(vocab).cuda()].cpu().numpy()
+    e = rel_fro(got_dw, ref_dw)
+    assert e <= BF["grad"], f"dW sampled vocab rows {e}{extra}"
+
+
+@pytest.fixture(scope="module")
+def c2():
+    x = I.make_workload("sft_bf16_T8192_d2560_V151936")
+    lse, logp = O.rows_lse_logp(x["H"], x["W"], x["labels"], None, IGN)
+    x["lse"], x["logp"] = lse, logp
+    return x
+
+
+@pytest.mark.parametrize("chunk", [512, 1024, 2048])
+def test_sft_T8192_d2560(sbp, c2, chunk):
+    H, W, y = c2["H"], c2["W"], c2["labels"]
+    valid = y != IGN
+    N = int(valid.sum())
+    ref_loss = -c2["logp"][valid].sum() / N
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    out = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    assert int(out["n_valid"].item()) == N
+    assert rel(out["loss"].item(), ref_loss) <= BF["loss"]
+    lp = out["logp"].cpu().numpy()
+    assert np.max(np.abs(lp - c2["logp"])) <= BF["logp"] * np.abs(c2["logp"]).max()
+    w = np.where(valid, 1.0 / N, 0.0)
+    rows = I.sample_rows(len(y), 256, 1001)
+    check_sampled(H, W, y, w, c2["lse"], out, rows, vocab_sample(y, W.shape[0], chunk), f" chunk={chunk}")
+
+
+def test_grpo_8x2048_d4096(sbp):
+    x = I.make_workload("grpo_bf16_8x2048_d4096_V151936")
+    H, W, y = x["H"], x["W"], x["labels"]
+    lse, logp = O.rows_lse_logp(H, W, y, None, IGN)
+    valid = y != IGN
+    lpo = (logp + x["logp_noise"]).astype(np.float32)      # old log-probs fixed at generation
+    A = x["advantages"].astype(np.float32)
+    N = int(valid.sum())
+    o, gar = O.grpo_weight(logp, lpo.astype(np.float64), A.astype(np.float64), valid)
+    ref_loss = -o.sum() / N
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    out = sbp.grpo(Ht, Wt, yt, torch.from_numpy(A).cuda(), torch.from_numpy(lpo).cuda(), 2048)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    assert int(out["n_valid"].item()) == N
+    assert rel(out["loss"].item(), ref_loss) <= BF["loss"]
+    check_sampled(H, W, y, gar / N, lse, out, I.sample_rows(len(y), 256, 1002), vocab_sample(y, W.shape[0], 3))
+
+
+def test_dpo_8x4096_d4096(sbp):
+    x = I.make_workload("dpo_bf16_8x4096_d4096_V151936")
+    H, W, y, cu, Sref = x["H"], x["W"], x["labels"], x["cu_seqlens"], x["ref_seq_logp"]
+    lse, logp = O.rows_lse_logp(H, W, y, None, IGN)
+    valid = y != IGN
+    S = O.seq_sums(logp, valid, cu)
+    m, ref_loss, wseq = O.dpo_scales(S, Sref, 0.1)
+    sid = O.seq_index(cu, len(y))
+    w = np.where(valid & (sid >= 0), wseq[np.maximum(sid, 0)], 0.0)
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    cut = torch.from_numpy(cu).cuda()
+    p1 = sbp.dpo_pass1(Ht, Wt, yt, cut, 2048)
+    p2 = sbp.dpo_pass2(Ht, Wt, yt, cut, p1["seq_logp"], torch.from_numpy(Sref).cuda(), 0.1, 2048)
+    torch.cuda.synchronize()
+    sbp.check_status(p1["status"])
+    sbp.check_status(p2["status"])
+    Sg = p1["seq_logp"].cpu().numpy()
+    assert np.max(np.abs(Sg - S) / np.abs(S)) <= BF["seq"]
+    assert rel(p2["loss"].item(), ref_loss) <= BF["loss"]
+    check_sampled(H, W, y, w, lse, p2, I.sample_rows(len(y), 256, 1003), vocab_sample(y, W.shape[0], 4))
+
+
+@pytest.fixture(scope="module")
+def c5():
+    return I.make_workload("sft_bf16_T65536_d5120_V151936")
+
+
+@pytest.mark.parametrize("chunk", [512, 1024, 2048, 4096, 8192])
+def test_sft_T65536_d5120_sampled(sbp, c5, chunk):
+    H, W, y = c5["H"], c5["W"], c5["labels"]
+    valid = y != IGN
+    N = int(valid.sum())
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    out = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    peak_extra = torch.cuda.max_memory_allocated() - base
+    T, V, d = H.shape[0], W.shape[0], H.shape[1]
+    # device memory beyond the inputs: dH, dW, the outputs and one chunk's workspace --
+    # far below the unchunked fp32 logits (T x V x 4 = 39.8 GB)
+    ws = sbp.workspace_bytes(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT)
+    assert peak_extra <= T * d * 2 + V * d * 4 + ws + 64 * T + (1 << 24)
+    assert peak_extra < T * V * 4 / 4
+    assert int(out["n_valid"].item()) == N
+    rows = I.sample_rows(T, 4096, 1004)
+    lse_s, logp_s = O.rows_lse_logp(H, W, y, rows, IGN)
+    lp = out["logp"].cpu().numpy()
+    assert np.max(np.abs(lp[rows] - logp_s)) <= BF["logp"] * np.abs(logp_s).max()
+    # the loss is the mean of the per-token terms (a property at any size)
+    assert rel(out["loss"].item(), -lp[valid].astype(np.float64).sum() / N) <= 1e-5
+    sub = rows[:: 8]
+    w = np.where(valid, 1.0 / N, 0.0)
+    ref_dh = O.rows_dH(H, W, y, w, sub, IGN)
+    got = out["dH"][torch.from_numpy(sub).cuda()].float().cpu().numpy()
+    assert rel_fro(got, ref_dh) <= BF["grad"]
+    assert torch.count_nonzero(out["dH"][torch.from_numpy(~valid).cuda()]).item() == 0
+
+
+def test_sft_T65536_d5120_prefix_full_dW(sbp, c5):
+    Tp = 4096
+    H, W, y = c5["H"][:Tp], c5["W"], c5["labels"][:Tp]
+    Ht, Wt, yt = dev_inputs(np.ascontiguousarray(H), W, np.ascontiguousarray(y))
+    out = sbp.sft(Ht, Wt, yt, 2048)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.sft(H, W, y, IGN)
+    assert rel(out["loss"].item(), ref["loss"]) <= BF["loss"]
+    assert rel_fro(out["dH"].float().cpu().numpy(), ref["dH"]) <= BF["grad"]
+    assert rel_fro(out["dW"].cpu().numpy(), ref["dW"]) <= BF["grad"]
