@@ -35,6 +35,10 @@ WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T16384_d4096_V151936_chunk2048", ob
 METRIC = "lm_head fwd+bwd tokens/s (SFT CE, d=4096, V=151936) and % BF16 tensor peak"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# A small case of the same kernels for ncu captures: inputs larger than L2 (W 268 MB)
+# but about 1.5 GB on the device in total.
+PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T2048_d4096_V32768_chunk2048", objective="sft", T=2048,
+                        d=4096, V=32768, chunk=2048, dtype="bf16", seed=1002, mask="frac", frac=0.1)
 CPU_SAMPLE_TOKENS = 384
 
 
@@ -319,7 +323,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w["workload"], "objective": "sft", "T": T, "d": d, "V": V, "chunk": chunk,
                    "tokens_per_gpu_per_step": T, "ignored_frac": w["frac"],
-                   "l2": "inputs larger than L2 (W 1.24 GB; chunk logits 0.62 GB per chunk)",
+                   "l2": f"inputs larger than L2 (W {V * d * 2 / 1e9:.2f} GB; chunk logits "
+                         f"{chunk * V * 2 / 1e9:.2f} GB per chunk)",
                    "parallelism": f"dp{world} replicas (no collective)"},
         "roofline": {"kernel": "k_bwd (dH and dW GEMMs of one chunk)", "bound": "tensor",
                      "achieved": bwd_tf, "peak": peak_tf, "unit": "TFLOP/s",
@@ -358,11 +363,17 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["main", "profile"], default="main",
+                    help="profile: a small case of the same kernels for ncu captures")
     args = ap.parse_args(argv)
+    if args.workload == "profile":
+        WORKLOAD.clear()
+        WORKLOAD.update(PROFILE_WORKLOAD)
+        args.no_cpu_baseline = True
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
