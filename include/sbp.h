@@ -63,6 +63,7 @@ extern "C" {
 #define SBP_ERR_TIMEOUT 5       /* (device) a kernel pipeline wait exceeded its limit      */
 #define SBP_ERR_CUDA 6          /* a CUDA runtime call failed (launch, memset, ...)       */
 #define SBP_ERR_UNSUPPORTED 7   /* shape the kernels do not handle (see dtype rules)       */
+#define SBP_ERR_SCRATCH_LIMIT 8 /* sizes need more scratch than sbp_lmhead_sft_noalloc has */
 
 /* operand dtypes */
 #define SBP_BF16 0
@@ -144,6 +145,33 @@ int sbp_lmhead_dpo_pass2(const void* H, const void* W, const int32_t* labels,
  * Events are created once and reused; no device memory is allocated. */
 int sbp_profile_enable(int on);
 int sbp_profile_read(double* ms, int64_t* launches, int n);
+
+/* Size of the fixed scratch array that sbp_lmhead_sft_noalloc works in (bytes). */
+#define SBP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* SFT cross-entropy exactly as sbp_lmhead_sft, for callers that cannot allocate device
+ * memory: it takes no workspace.  (The paper has no counterpart; this is a library
+ * convenience.)  Some callers have no way to get scratch memory of their own -- code
+ * that runs inside a host framework or plugin that owns every allocation and offers
+ * none to extensions, a fixed-budget runtime that forbids allocating on its hot path
+ * (an allocation can also synchronise the device), or plain C callers without an
+ * allocator.  They pass only inputs and outputs, and the call works in one statically
+ * sized device array of SBP_NOALLOC_SCRATCH_BYTES (64 MiB) that the library defines;
+ * every GPU that loads the library holds that array until the process exits.
+ * Sizes whose workspace (sbp_lmhead_workspace_bytes with SBP_MODE_SFT) exceeds it are
+ * rejected on the host with SBP_ERR_SCRATCH_LIMIT before anything is enqueued; with
+ * V = 151936 and d = 4096, chunks up to about 96 rows fit.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls share the one
+ * array: calls that overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  Other arguments, outputs and errors as
+ * sbp_lmhead_sft. */
+int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels,
+                           int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                           int dtype, float* loss, int64_t* n_valid, float* logp_out,
+                           void* dH, float* dW, int accumulate_dW,
+                           int32_t* dev_status, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* sbp_status_string(int status);

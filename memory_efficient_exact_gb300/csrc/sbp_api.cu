@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <vector>
 
 #include "sbp_internal.h"
@@ -589,6 +590,34 @@ int run(const Call& c) {
 }
 
 }  // namespace
+
+// Scratch of sbp_lmhead_sft_noalloc: a fixed device array in this module, so that
+// callers without an allocator can still run the chunked LM head.  Every GPU that
+// loads the library holds it until the process exits; all calls share it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SBP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once per
+// device (cudaGetSymbolAddress, with that device current) and cached.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SBP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SBP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SBP_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SBP_OK;
+}
+}  // namespace
 }  // namespace sbp
 
 using namespace sbp;
@@ -656,6 +685,26 @@ int sbp_lmhead_dpo_pass2(const void* H, const void* W, const int32_t* labels, co
   return run(c);
 }
 
+int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels, int64_t T, int64_t d, int64_t V,
+                           int64_t chunk, int32_t ignore_index, int dtype, float* loss, int64_t* n_valid,
+                           float* logp_out, void* dH, float* dW, int accumulate_dW, int32_t* dev_status,
+                           void* stream) {
+  if (!loss) return SBP_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(T, d, V, chunk, dtype, SBP_MODE_SFT, &L)) return SBP_ERR_INVALID_ARG;
+  if (L.total > (size_t)SBP_NOALLOC_SCRATCH_BYTES) return SBP_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != SBP_OK) return st;
+  Call c{};
+  c.mode = SBP_MODE_SFT; c.H = H; c.W = W; c.labels = labels; c.T = T; c.d = d; c.V = V; c.chunk = chunk;
+  c.ign = ignore_index; c.dtype = dtype; c.loss = loss; c.n_valid = n_valid; c.logp_out = logp_out;
+  c.dH = dH; c.dW = dW; c.accumulate_dW = accumulate_dW; c.ws = scratch;
+  c.ws_bytes = (size_t)SBP_NOALLOC_SCRATCH_BYTES; c.dev_status = dev_status;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
 const char* sbp_status_string(int status) {
   switch (status) {
     case SBP_OK: return "SBP_OK";
@@ -666,6 +715,7 @@ const char* sbp_status_string(int status) {
     case SBP_ERR_TIMEOUT: return "SBP_ERR_TIMEOUT";
     case SBP_ERR_CUDA: return "SBP_ERR_CUDA";
     case SBP_ERR_UNSUPPORTED: return "SBP_ERR_UNSUPPORTED";
+    case SBP_ERR_SCRATCH_LIMIT: return "SBP_ERR_SCRATCH_LIMIT";
     default: return "SBP_ERR_UNKNOWN";
   }
 }

@@ -18,7 +18,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsbp.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "sbp.h")
 
-OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_LABEL_RANGE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED = range(8)
+(OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_LABEL_RANGE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED,
+ ERR_SCRATCH_LIMIT) = range(9)
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 BF16, FP32 = 0, 1
 MODE_SFT, MODE_GRPO, MODE_DPO1, MODE_DPO2 = 0, 1, 2, 3
 IGNORE_INDEX = -100
@@ -48,6 +50,8 @@ def _load() -> ctypes.CDLL:
     lib.sbp_lmhead_dpo_pass2.restype = C
     lib.sbp_lmhead_dpo_pass2.argtypes = [P, P, P, P, I32, P, P, F, I64, I64, I64, I64, I32, C, P, P, P, P, C, P,
                                          SZ, P, P]
+    lib.sbp_lmhead_sft_noalloc.restype = C
+    lib.sbp_lmhead_sft_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, P]
     lib.sbp_status_string.restype = ctypes.c_char_p
     lib.sbp_status_string.argtypes = [C]
     lib.sbp_last_launch_count.restype = C
@@ -170,6 +174,32 @@ def sft(H, W, labels, chunk, ignore_index=IGNORE_INDEX, *, dH=None, dW=None, acc
     _check(_lib.sbp_lmhead_sft(_p(H), _p(W), _p(labels), T, d, V, chunk, ignore_index, dt, _p(loss), _p(nv),
                                _p(lp), _p(dH), _p(dW), int(bool(accumulate_dW)), _p(ws), ws.numel(), _p(st),
                                _stream(stream)), "sbp_lmhead_sft")
+    return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
+
+
+def sft_noalloc(H, W, labels, chunk, ignore_index=IGNORE_INDEX, *, dH=None, dW=None, accumulate_dW=False,
+                logp=True, status=None, stream=None) -> dict:
+    """SFT forward + backward without a workspace (``sbp_lmhead_sft_noalloc``): for
+    callers that cannot allocate device scratch.  The library works in its own fixed
+    64 MiB device array, shared by all calls (overlapping calls race).  Output tensors
+    are still the caller's."""
+    _dev(H, W, labels)
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    T, d = H.shape
+    V = W.shape[0]
+    if W.shape[1] != d or H.dtype != W.dtype or labels.shape != (T,):
+        raise ValueError("shape/dtype mismatch between H [T,d], W [V,d], labels [T]")
+    dt = _code(H)
+    dH, dW = _grad_out(H, W, dH, dW)
+    dev = H.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    nv = torch.empty((), dtype=torch.int64, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev) if logp else None
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_lmhead_sft_noalloc(_p(H), _p(W), _p(labels), T, d, V, chunk, ignore_index, dt, _p(loss),
+                                       _p(nv), _p(lp), _p(dH), _p(dW), int(bool(accumulate_dW)), _p(st),
+                                       _stream(stream)), "sbp_lmhead_sft_noalloc")
     return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
 
 
