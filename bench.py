@@ -307,7 +307,7 @@ def run_ours(args):
     fwd_tf = flops_fwd_launch / fwd_avg_s / 1e12 if fwd_n else None
     peak_tf = peaks["bf16_tflops_sustained"]
     useful_tf = 6.0 * d * V * value / 1e12
-    gtb = 2.0 * chunk * V * 2 * 2 / 1e9  # logit gradient: read e (fp16) + write G (bf16)
+    gtb = 4.0 * chunk * V / 1e9  # logit gradient: read e (fp16) + write G (bf16), bytes per launch
     grad_gbs = gtb / (grad_ms / max(grad_n, 1) / 1000.0) if grad_n else None
 
     cpu = None

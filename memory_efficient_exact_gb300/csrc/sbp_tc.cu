@@ -566,13 +566,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (cg + 32 <= p.d) {
           float4* o4 = reinterpret_cast<float4*>(o);
           if (add) {
-            float4 old[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) old[k] = o4[k];
+            // dW += acc as fire-and-forget vector reductions performed in L2: the
+            // epilogue never waits on a load.  Each dW element receives exactly one
+            // add per launch (one unit owns each tile), so the result is the same
+            // single fp32 addition as a load-add-store, and deterministic.
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              o4[k] = make_float4(old[k].x + __uint_as_float(r[4 * k]), old[k].y + __uint_as_float(r[4 * k + 1]),
-                                  old[k].z + __uint_as_float(r[4 * k + 2]), old[k].w + __uint_as_float(r[4 * k + 3]));
+              atomicAdd(o4 + k, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                            __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
           } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -582,7 +583,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (cg + j < p.d) o[j] = add ? o[j] + __uint_as_float(r[j]) : __uint_as_float(r[j]);
+            if (cg + j < p.d) {
+              if (add) atomicAdd(o + j, __uint_as_float(r[j]));
+              else o[j] = __uint_as_float(r[j]);
+            }
         }
       }
       tc_fence_before();

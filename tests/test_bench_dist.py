@@ -1,0 +1,58 @@
+"""The multi-rank bench path on CPU: world size 2 over gloo.
+
+Every rank runs its own batch (weak scaling, no collective on the data path); the
+bench reports whole-job tokens (sum over ranks) over the step time (max over ranks).
+"""
+import os
+import socket
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, lr = bench.dist_env()
+    tokens, ms = bench.aggregate(torch, dist, 1000.0 * (rank + 1), 10.0 + 5.0 * rank, "cpu")
+    # per-rank inputs differ (seed + rank) but have the same shape
+    from memory_efficient_exact_gb300 import inputs as I
+    y = I.make_labels(64, 100, 1002 + rank, "frac", 0.1)
+    q.put((rank, r, w, tokens, ms, int((y == -100).sum()), y[:8].tolist()))
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, r, w, tokens, ms, n_ign, head in res:
+        assert r == rank and w == 2
+        assert tokens == 3000.0          # sum over ranks
+        assert ms == 15.0                # max over ranks
+        assert n_ign == 6                # floor(0.1 * 64) on every rank
+    assert res[0][6] != res[1][6]        # each rank draws its own batch

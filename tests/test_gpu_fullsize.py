@@ -126,7 +126,14 @@ def test_dpo_8x4096_d4096(sbp):
 
 @pytest.fixture(scope="module")
 def c5():
-    return I.make_workload("sft_bf16_T65536_d5120_V151936")
+    x = I.make_workload("sft_bf16_T65536_d5120_V151936")
+    H, W, y = x["H"], x["W"], x["labels"]
+    valid = y != IGN
+    x["rows"] = I.sample_rows(H.shape[0], 4096, 1004)
+    x["lse_s"], x["logp_s"] = O.rows_lse_logp(H, W, y, x["rows"], IGN)
+    x["sub"] = x["rows"][::8]
+    x["ref_dh"] = O.rows_dH(H, W, y, np.where(valid, 1.0 / int(valid.sum()), 0.0), x["sub"], IGN)
+    return x
 
 
 @pytest.mark.parametrize("chunk", [512, 1024, 2048, 4096, 8192])
@@ -148,17 +155,13 @@ def test_sft_T65536_d5120_sampled(sbp, c5, chunk):
     assert peak_extra <= T * d * 2 + V * d * 4 + ws + 64 * T + (1 << 24)
     assert peak_extra < T * V * 4 / 4
     assert int(out["n_valid"].item()) == N
-    rows = I.sample_rows(T, 4096, 1004)
-    lse_s, logp_s = O.rows_lse_logp(H, W, y, rows, IGN)
+    rows, logp_s = c5["rows"], c5["logp_s"]
     lp = out["logp"].cpu().numpy()
     assert np.max(np.abs(lp[rows] - logp_s)) <= BF["logp"] * np.abs(logp_s).max()
     # the loss is the mean of the per-token terms (a property at any size)
     assert rel(out["loss"].item(), -lp[valid].astype(np.float64).sum() / N) <= 1e-5
-    sub = rows[:: 8]
-    w = np.where(valid, 1.0 / N, 0.0)
-    ref_dh = O.rows_dH(H, W, y, w, sub, IGN)
-    got = out["dH"][torch.from_numpy(sub).cuda()].float().cpu().numpy()
-    assert rel_fro(got, ref_dh) <= BF["grad"]
+    got = out["dH"][torch.from_numpy(c5["sub"]).cuda()].float().cpu().numpy()
+    assert rel_fro(got, c5["ref_dh"]) <= BF["grad"]
     assert torch.count_nonzero(out["dH"][torch.from_numpy(~valid).cuda()]).item() == 0
 
 
