@@ -299,15 +299,17 @@ def run_ours(args):
     fwd_ms, fwd_n = prof["forward_gemm"]
     grad_ms, grad_n = prof["logit_grad"]
     oth_ms, oth_n = prof["other"]
-    flops_bwd_launch = 4.0 * chunk * d * V          # dH and dW GEMMs of one chunk (algorithmic)
-    flops_fwd_launch = 2.0 * chunk * d * V
+    # algorithmic FLOPs per launch (average over the chunks of a call): dH and dW GEMMs
+    # of one chunk = 4 rows d V; the forward GEMM = 2 rows d V
+    flops_bwd_launch = 4.0 * T * d * V / n_chunks
+    flops_fwd_launch = 2.0 * T * d * V / n_chunks
     bwd_avg_s = bwd_ms / max(bwd_n, 1) / 1000.0
     fwd_avg_s = fwd_ms / max(fwd_n, 1) / 1000.0
     bwd_tf = flops_bwd_launch / bwd_avg_s / 1e12 if bwd_n else None
     fwd_tf = flops_fwd_launch / fwd_avg_s / 1e12 if fwd_n else None
     peak_tf = peaks["bf16_tflops_sustained"]
     useful_tf = 6.0 * d * V * value / 1e12
-    gtb = 4.0 * chunk * V / 1e9  # logit gradient: read e (fp16) + write G (bf16), bytes per launch
+    gtb = 4.0 * (T / n_chunks) * V / 1e9  # logit gradient: read e (fp16) + write G (bf16), GB per launch
     grad_gbs = gtb / (grad_ms / max(grad_n, 1) / 1000.0) if grad_n else None
 
     cpu = None
@@ -369,11 +371,20 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["main", "profile"], default="main",
                     help="profile: a small case of the same kernels for ncu captures")
+    ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
+    ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
+    ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
     args = ap.parse_args(argv)
     if args.workload == "profile":
         WORKLOAD.clear()
         WORKLOAD.update(PROFILE_WORKLOAD)
         args.no_cpu_baseline = True
+    for key, val in (("chunk", args.chunk), ("T", args.tokens), ("d", args.d)):
+        if val is not None:
+            WORKLOAD[key] = val
+    if args.chunk is not None or args.tokens is not None or args.d is not None:
+        WORKLOAD["workload"] = (f"sft_ce_lmhead_bf16_T{WORKLOAD['T']}_d{WORKLOAD['d']}_V{WORKLOAD['V']}"
+                                f"_chunk{WORKLOAD['chunk']}")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

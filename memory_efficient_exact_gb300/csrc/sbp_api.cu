@@ -76,10 +76,11 @@ int num_sms() {
 // stay below a quarter of the average per-SM work so the short dW units can even
 // out the finish times.
 int choose_splits(int64_t rows, int64_t d, int64_t V, int sms) {
-  const int64_t mt_c = (rows + 127) / 128, nt_d = (d + 255) / 256, kb_v = (V + 63) / 64;
-  const int64_t mt_v = (V + 127) / 128, kb_c = (rows + 63) / 64;
+  // units are 256-row tiles computed by SM pairs
+  const int64_t mt_c = (rows + 255) / 256, nt_d = (d + 255) / 256, kb_v = (V + 63) / 64;
+  const int64_t mt_v = (V + 255) / 256, kb_c = (rows + 63) / 64;
   const double total = double(mt_c * nt_d * kb_v + mt_v * nt_d * kb_c);
-  const double per_sm = total / double(sms > 0 ? sms : 148);
+  const double per_sm = total / double(sms > 1 ? sms / 2 : 74);
   int s = (int)std::ceil(4.0 * double(kb_v) / (per_sm > 1.0 ? per_sm : 1.0));
   if (s < 1) s = 1;
   if (s > 16) s = 16;

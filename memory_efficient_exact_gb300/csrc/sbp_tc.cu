@@ -1,9 +1,15 @@
 // Tensor-core (tcgen05 / TMEM / TMA) kernels of the bf16 LM-head path, sm_103a.
 //
-// Both kernels are persistent, warp-specialised GEMMs with 128x256 fp32 accumulators in
-// tensor memory (two buffers, 512 columns) and a 4-stage TMA -> shared-memory ring:
+// Both kernels are persistent, warp-specialised GEMMs run by clusters of two CTAs on two
+// SMs ("pairs").  A pair computes one 256x256 fp32 tile with tcgen05.mma.cta_group::2:
+// CTA r of the pair stages rows [128r, 128r+128) of A and rows [128r, 128r+128) of B's N
+// extent through a 6-stage TMA -> shared-memory ring (32 KB per 64-deep k-block), the
+// leader (r = 0) issues the MMAs, and each CTA's tensor memory receives its own 128
+// accumulator rows x 256 columns (two buffers, 512 columns).  Per SM this moves a third
+// less data through shared memory and L2 than a 1-SM 128x256 tile, whose operand
+// traffic exceeds what the SM's shared memory delivers.  Roles per CTA:
 //   warp 0      TMA producer (one lane)
-//   warp 1      TMEM allocator + MMA issuer (one lane issues tcgen05.mma)
+//   warp 1      TMEM allocator; in the leader, the MMA issuer (one lane)
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).. (one accumulator row per
 //               thread) and columns [128*h, 128*h+128) of the tile, h = (w-2)/4.
 //
@@ -33,28 +39,13 @@
 namespace sbp {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BN = 256, BK = 64;
 constexpr uint32_t BOX_BYTES = 64 * 64 * 2; // one 64x64 bf16 box (MN-major operands)
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int RING = 4;
 constexpr float L2E = 1.4426950408889634f;
-
-struct Ctrl {
-  uint64_t full[STAGES], empty[STAGES];
-  uint64_t tfull[2], tempty[2];
-  uint64_t rfull[RING], rempty[RING];
-  uint64_t mdone;
-  int ring[RING];
-  uint32_t tmem_base;
-  int abort;
-};
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9, 10-12 = 1), A / B major-ness (bit 15 / 16: 0 = K-major, 1 = MN-major),
@@ -63,9 +54,6 @@ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t IDESC_FWD = idesc_bf16(BM, BN, false, false);
-constexpr uint32_t IDESC_DH = idesc_bf16(BM, BN, false, true);
-constexpr uint32_t IDESC_DW = idesc_bf16(BM, BN, true, true);
 
 // ------------------------------------------------------------------------------ PTX helpers
 
@@ -177,66 +165,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void fail(Ctrl* c, int32_t* status) {
-  *(volatile int*)&c->abort = 1;
-  if (status) atomicCAS(status, 0, SBP_ERR_TIMEOUT);
-}
-
-// Warp-uniform bounded wait: all lanes poll, the warp proceeds only if every lane saw
-// the phase complete.
-__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, Ctrl* c, uint64_t limit) {
-  const bool ok = wait_bounded(b, parity, &c->abort, limit);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Common prologue: barrier init, TMEM allocation (warp 1), and the hand-off of the
-// TMEM base address to all warps.
-__device__ __forceinline__ void prologue(Ctrl* c, int warp) {
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&c->full[i], 1);
-      mbar_init(&c->empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&c->tfull[i], 1);
-      mbar_init(&c->tempty[i], NUM_EPI_WARPS * 32);
-    }
-    for (int i = 0; i < RING; ++i) {
-      mbar_init(&c->rfull[i], 1);
-      mbar_init(&c->rempty[i], 1 + NUM_EPI_WARPS);
-    }
-    mbar_init(&c->mdone, 1);
-    c->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 1) tmem_alloc(&c->tmem_base, TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-}
-
-// Producer teardown after an abort: wait (bounded, ignoring the abort flag) until every
-// copy it issued has landed, so no TMA write is pending when the CTA exits.
-__device__ __forceinline__ void drain_copies(Ctrl* c, const uint32_t* last_phase, uint32_t issued_mask) {
-  for (int s = 0; s < STAGES; ++s)
-    if (issued_mask & (1u << s)) wait_bounded(&c->full[s], last_phase[s], nullptr, 200000000ull);
-}
-
-// MMA teardown: a final commit tracks every MMA this thread issued; wait for it.
-__device__ __forceinline__ void drain_mma(Ctrl* c) {
-  mma_commit(&c->mdone);
-  wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
-}
-
-__device__ __forceinline__ void epilogue_teardown(Ctrl* c, int warp) {
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(c->tmem_base, TMEM_COLS);
-  }
-}
-
 // ==================================================================================== forward
 
 struct FwdP {
@@ -248,31 +176,212 @@ struct FwdP {
   int32_t* status; uint64_t limit_ns;
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// =================================================================================== backward
+
+struct BwdP {
+  int rows; int64_t r0; int64_t V, d;
+  int mt_c, nt_d, kb_v, splits, mt_v, kb_c;
+  int n_dh, n_total;
+  float* dh_part; int64_t plane;
+  float* dW; int dw_acc;
+  uint32_t* counter;
+  int32_t* status; uint64_t limit_ns;
+};
+
+// ============================================================================ pair protocol
+//   full[s]   (leader only) completes when both CTAs' TMA copies of stage s landed: the
+//             leader expects 64 KB, the peer's copies complete on it across the pair
+//   empty[s]  (both) the leader's MMA commit, multicast to the pair, frees stage s
+//   tfull[b]  (both) the leader's commit, multicast: accumulator b is ready
+//   tempty[b] (leader) all 16 epilogue warps of the pair drained accumulator b
+//   rfull/rempty  the work queue of k_bwd: the leader takes a unit and writes it into
+//             both CTAs' rings (distributed shared memory)
+
+constexpr int STAGES = 6;
+constexpr uint32_t A_BYTES = 128 * BK * 2;   // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t B_BYTES = 128 * BK * 2;   // 16 KB: this CTA's 128 rows of B
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;  // bytes that complete one leader full barrier
+constexpr uint32_t IDESC_FWD = idesc_bf16(256, 256, false, false);
+constexpr uint32_t IDESC_DH = idesc_bf16(256, 256, false, true);
+constexpr uint32_t IDESC_DW = idesc_bf16(256, 256, true, true);
+
+struct Ctrl {
+  uint64_t full[STAGES], empty[STAGES];
+  uint64_t tfull[2], tempty[2];
+  uint64_t rfull[RING], rempty[RING];
+  uint64_t mdone;
+  int ring[RING];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+
+__device__ __forceinline__ uint32_t ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool try_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (barriers that remote CTAs arrive on).
+__device__ __noinline__ bool wait_cluster_slow(uint64_t* b, uint32_t parity, const volatile int* abort_flag,
+                                               uint64_t limit_ns) {
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (try_cluster(b, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (gtimer() - t0 > limit_ns) return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_cluster(uint64_t* b, uint32_t parity, const volatile int* abort_flag,
+                                             uint64_t limit_ns) {
+  if (try_cluster(b, parity)) return true;
+  return wait_cluster_slow(b, parity, abort_flag, limit_ns);
+}
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* b, uint32_t parity, Ctrl* c, uint64_t limit) {
+  const bool ok = wait_cluster(b, parity, &c->abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an mbarrier
+// that may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Arrive (once the MMAs issued so far complete) on the barrier at this offset in every
+// CTA of `mask`.
+__device__ __forceinline__ void commit2_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   saddr(bar)),
+               "h"(mask)
+               : "memory");
+}
+
+__device__ __forceinline__ void fail(Ctrl* c, int32_t* status) {
+  *(volatile int*)&c->abort = 1;
+  if (status) atomicCAS(status, 0, SBP_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ void prologue(Ctrl* c, int warp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&c->full[i], 1);
+      mbar_init(&c->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->tfull[i], 1);
+      mbar_init(&c->tempty[i], 2 * NUM_EPI_WARPS);
+    }
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&c->rfull[i], 1);
+      // leader: its MMA thread and epilogue warps, the peer's producer and epilogue warps
+      mbar_init(&c->rempty[i], 2 + 2 * NUM_EPI_WARPS);
+    }
+    mbar_init(&c->mdone, 1);
+    c->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&c->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+}
+
+__device__ __forceinline__ void drain_copies(Ctrl* c, const uint32_t* last_phase, uint32_t issued_mask) {
+  for (int s = 0; s < STAGES; ++s)
+    if (issued_mask & (1u << s)) wait_bounded(&c->full[s], last_phase[s], nullptr, 200000000ull);
+}
+
+__device__ __forceinline__ void teardown(Ctrl* c, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(c->tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// Epilogue arrival on the leader's tempty[buf]: one per warp.
+__device__ __forceinline__ void release_tmem(Ctrl* c, int buf, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) arrive_cluster(mapa(saddr(&c->tempty[buf]), 0));
+}
+
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW, const FwdP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ctarank();
   prologue(c, warp);
   const uint32_t tmem = c->tmem_base;
-  const int total = p.mt * p.ntn;
+  const int mtp = (p.rows + 255) / 256;
+  const int total = mtp * p.ntn;
+  const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0) {
     if (lane == 0) {
       prefetch_map(&tmH);
       prefetch_map(&tmW);
       int stage = 0;
-      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0};
+      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0, 0, 0};
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const int mb = tile % p.mt, nb = tile / p.mt;
+      for (int tile = pid; tile < total && ok; tile += npairs) {
+        const int mp = tile % mtp, nb = tile / mtp;
+        const int arow = (int)(p.r0 + (int64_t)mp * 256 + rank * 128);
+        const int brow = nb * BN + (int)rank * 128;
         for (int kb = 0; kb < p.kb; ++kb) {
           if (!wait_bounded(&c->empty[stage], phase ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
-          mbar_expect_tx(&c->full[stage], STAGE_BYTES);
-          tma_load_2d(sa, &tmH, &c->full[stage], kb * BK, (int)(p.r0 + (int64_t)mb * BM));
-          tma_load_2d(sb, &tmW, &c->full[stage], kb * BK, nb * BN);
+          const uint32_t fb = mapa(saddr(&c->full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&c->full[stage], PAIR_TX);
+          tma_load_2d_pair(sa, &tmH, fb, kb * BK, arow);
+          tma_load_2d_pair(sb, &tmW, fb, kb * BK, brow);
           issued |= 1u << stage;
           last_phase[stage] = phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -280,18 +389,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) {
         fail(c, p.status);
-        drain_copies(c, last_phase, issued);
+        if (rank == 0) drain_copies(c, last_phase, issued);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0, local = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++local) {
+      for (int tile = pid; tile < total && ok; tile += npairs, ++local) {
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!wait_bounded(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        if (!wait_cluster(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)(buf * BN);
         for (int kb = 0; kb < p.kb; ++kb) {
@@ -300,30 +409,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), sw128_desc(sb + k * 32, 16, 1024), IDESC_FWD,
-                     (kb | k) != 0);
-          mma_commit(&c->empty[stage]);
+            mma2_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), sw128_desc(sb + k * 32, 16, 1024), IDESC_FWD,
+                      (kb | k) != 0);
+          commit2_mc(&c->empty[stage], 3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&c->tfull[buf]);
+        commit2_mc(&c->tfull[buf], 3);
       }
       if (!ok) fail(c, p.status);
-      drain_mma(c);
+      commit2_mc(&c->mdone, 1);
+      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
     }
     __syncwarp();
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int lrow = q * 32 + lane;
     int local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const int mb = tile % p.mt, nb = tile / p.mt;
+    for (int tile = pid; tile < total; tile += npairs, ++local) {
+      const int mp = tile % mtp, nb = tile / mtp;
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      const int row = mb * BM + lrow;
+      const int row = mp * 256 + (int)rank * 128 + lrow;
       const bool vrow = row < p.rows;
       const int32_t y = vrow ? p.labels[row] : INT_MIN;
-      if (!warp_wait(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
+      if (!warp_wait_cluster(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
         fail(c, p.status);
         break;
       }
@@ -371,38 +481,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 4; ++k) dst[k] = make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&c->tempty[buf]);
+      release_tmem(c, buf, lane);
       const int64_t tix = (int64_t)nb * 2 + h;
       if (vrow && tix < p.ntiles) p.part[(int64_t)row * p.ntiles + tix] = make_float2(m, s);
       if (vrow && has_y) p.zy[row] = zyv;
     }
   }
-  epilogue_teardown(c, warp);
+  teardown(c, warp);
 }
 
-// =================================================================================== backward
-
-struct BwdP {
-  int rows; int64_t r0; int64_t V, d;
-  int mt_c, nt_d, kb_v, splits, mt_v, kb_c;
-  int n_dh, n_total;
-  float* dh_part; int64_t plane;
-  float* dW; int dw_acc;
-  uint32_t* counter;
-  int32_t* status; uint64_t limit_ns;
-};
-
+// Backward, pair version.  Units are decoded from the same atomic queue as the 1-CTA
+// kernel, but M tiles are 256 rows (a pair) and the leader's producer takes each unit
+// from the queue and hands it to the peer through distributed shared memory.
 struct Unit {
-  int kind;   // 0 = dH, 1 = dW
-  int mb, nb, split, kb0, kb1;
+  int kind, mp, nb, split, kb0, kb1;
 };
 
 __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
   Unit w;
   if (u < p.n_dh) {
     w.kind = 0;
-    w.mb = u % p.mt_c;
+    w.mp = u % p.mt_c;
     w.nb = (u / p.mt_c) % p.nt_d;
     w.split = u / (p.mt_c * p.nt_d);
     w.kb0 = (int)((int64_t)w.split * p.kb_v / p.splits);
@@ -411,7 +510,7 @@ __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
     u -= p.n_dh;
     w.kind = 1;
     w.nb = u % p.nt_d;
-    w.mb = u / p.nt_d;
+    w.mp = u / p.nt_d;
     w.split = 0;
     w.kb0 = 0;
     w.kb1 = p.kb_c;
@@ -419,13 +518,14 @@ __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
   return w;
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_bwd(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmGmn,
-          const __grid_constant__ CUtensorMap tmWmn, const __grid_constant__ CUtensorMap tmHmn, const BwdP p) {
+               const __grid_constant__ CUtensorMap tmWmn, const __grid_constant__ CUtensorMap tmHmn, const BwdP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ctarank();
   prologue(c, warp);
   const uint32_t tmem = c->tmem_base;
 
@@ -436,33 +536,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       prefetch_map(&tmWmn);
       prefetch_map(&tmHmn);
       int stage = 0;
-      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0};
+      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0, 0, 0};
       bool ok = true;
       for (int i = 0; ok; ++i) {
         const int slot = i % RING;
         const uint32_t rph = (uint32_t)((i / RING) & 1);
-        if (!wait_bounded(&c->rempty[slot], rph ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
-        int u = (int)atomicAdd(p.counter, 1u);
-        if (u >= p.n_total) u = -1;
-        c->ring[slot] = u;
-        mbar_arrive(&c->rfull[slot]);
+        int u;
+        if (rank == 0) {
+          if (!wait_cluster(&c->rempty[slot], rph ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          u = (int)atomicAdd(p.counter, 1u);
+          if (u >= p.n_total) u = -1;
+          c->ring[slot] = u;
+          asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(saddr(&c->ring[slot]), 1)), "r"(u) : "memory");
+          mbar_arrive(&c->rfull[slot]);
+          arrive_cluster(mapa(saddr(&c->rfull[slot]), 1));
+        } else {
+          if (!wait_cluster(&c->rfull[slot], rph, &c->abort, p.limit_ns)) { ok = false; break; }
+          u = *(volatile int*)&c->ring[slot];
+          arrive_cluster(mapa(saddr(&c->rempty[slot]), 0));
+        }
         if (u < 0) break;
         const Unit w = decode(p, u);
+        const int mrow = w.mp * 256 + (int)rank * 128;      // this CTA's first M row (or V row)
+        const int ncol = w.nb * BN + (int)rank * 128;       // this CTA's first N column of d
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!wait_bounded(&c->empty[stage], phase ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
-          uint64_t* fb = &c->full[stage];
-          mbar_expect_tx(fb, STAGE_BYTES);
+          const uint32_t fb = mapa(saddr(&c->full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&c->full[stage], PAIR_TX);
           if (w.kind == 0) {
-            tma_load_2d(sa, &tmGk, fb, kb * BK, w.mb * BM);
+            tma_load_2d_pair(sa, &tmGk, fb, kb * BK, mrow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmWmn, fb, w.nb * BN + j * 64, kb * BK);
+            for (int j = 0; j < 2; ++j) tma_load_2d_pair(sb + j * BOX_BYTES, &tmWmn, fb, ncol + j * 64, kb * BK);
           } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * BOX_BYTES, &tmGmn, fb, w.mb * BM + j * 64, kb * BK);
+            for (int j = 0; j < 2; ++j) tma_load_2d_pair(sa + j * BOX_BYTES, &tmGmn, fb, mrow + j * 64, kb * BK);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(sb + j * BOX_BYTES, &tmHmn, fb, w.nb * BN + j * 64, (int)(p.r0 + (int64_t)kb * BK));
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(sb + j * BOX_BYTES, &tmHmn, fb, ncol + j * 64, (int)(p.r0 + (int64_t)kb * BK));
           }
           issued |= 1u << stage;
           last_phase[stage] = phase;
@@ -471,25 +582,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) {
         fail(c, p.status);
-        drain_copies(c, last_phase, issued);
+        if (rank == 0) drain_copies(c, last_phase, issued);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0, local = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int i = 0; ok; ++i, ++local) {
         const int slot = i % RING;
         const uint32_t rph = (uint32_t)((i / RING) & 1);
-        if (!wait_bounded(&c->rfull[slot], rph, &c->abort, p.limit_ns)) { ok = false; break; }
-        const int u = c->ring[slot];
+        if (!wait_cluster(&c->rfull[slot], rph, &c->abort, p.limit_ns)) { ok = false; break; }
+        const int u = *(volatile int*)&c->ring[slot];
         mbar_arrive(&c->rempty[slot]);
         if (u < 0) break;
         const Unit w = decode(p, u);
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!wait_bounded(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        if (!wait_cluster(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)(buf * BN);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -500,22 +611,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (w.kind == 0) {
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              mma_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), sw128_desc(sb + k * 2048, BOX_BYTES, 1024), IDESC_DH,
-                       acc0 | (k != 0));
+              mma2_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), sw128_desc(sb + k * 2048, BOX_BYTES, 1024), IDESC_DH,
+                        acc0 | (k != 0));
           } else {
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              mma_bf16(dt, sw128_desc(sa + k * 2048, BOX_BYTES, 1024), sw128_desc(sb + k * 2048, BOX_BYTES, 1024),
-                       IDESC_DW, acc0 | (k != 0));
+              mma2_bf16(dt, sw128_desc(sa + k * 2048, BOX_BYTES, 1024), sw128_desc(sb + k * 2048, BOX_BYTES, 1024),
+                        IDESC_DW, acc0 | (k != 0));
           }
-          mma_commit(&c->empty[stage]);
+          commit2_mc(&c->empty[stage], 3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&c->tfull[buf]);
+        commit2_mc(&c->tfull[buf], 3);
       }
       if (!ok) fail(c, p.status);
-      drain_mma(c);
+      commit2_mc(&c->mdone, 1);
+      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
     }
     __syncwarp();
   } else {
@@ -525,25 +637,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0;; ++i, ++local) {
       const int slot = i % RING;
       const uint32_t rph = (uint32_t)((i / RING) & 1);
-      if (!warp_wait(&c->rfull[slot], rph, c, p.limit_ns)) {
+      if (!warp_wait_cluster(&c->rfull[slot], rph, c, p.limit_ns)) {
         fail(c, p.status);
         break;
       }
-      const int u = c->ring[slot];
+      const int u = *(volatile int*)&c->ring[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c->rempty[slot]);
+      if (lane == 0) arrive_cluster(mapa(saddr(&c->rempty[slot]), 0));
       if (u < 0) break;
       const Unit w = decode(p, u);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      if (!warp_wait(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
+      if (!warp_wait_cluster(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
         fail(c, p.status);
         break;
       }
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
       const int64_t c0 = (int64_t)w.nb * BN + h * 128;
-      const int64_t row = (int64_t)w.mb * BM + lrow;
+      const int64_t row = (int64_t)w.mp * 256 + rank * 128 + lrow;
       float* dst;
       bool vrow;
       if (w.kind == 0) {
@@ -566,10 +678,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (cg + 32 <= p.d) {
           float4* o4 = reinterpret_cast<float4*>(o);
           if (add) {
-            // dW += acc as fire-and-forget vector reductions performed in L2: the
-            // epilogue never waits on a load.  Each dW element receives exactly one
-            // add per launch (one unit owns each tile), so the result is the same
-            // single fp32 addition as a load-add-store, and deterministic.
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               atomicAdd(o4 + k, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
@@ -589,11 +697,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&c->tempty[buf]);
+      release_tmem(c, buf, lane);
     }
   }
-  epilogue_teardown(c, warp);
+  teardown(c, warp);
 }
 
 // ======================================================================================= host
@@ -642,13 +749,41 @@ bool set_smem_attr() {
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   if (done == 0) {
-    const bool ok = cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) ==
-                        cudaSuccess &&
-                    cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) ==
-                        cudaSuccess;
+    const bool ok =
+        cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) == cudaSuccess &&
+        cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) == cudaSuccess;
     done = ok ? 1 : -1;
   }
   return done == 1;
+}
+
+// Clusters of two (SM pairs) that can be resident at once, cached per device and kernel.
+int max_pairs(const void* kernel) {
+  static int cache[64][2] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int which = kernel == (const void*)k_fwd ? 0 : 1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev >= 0 && dev < 64 && cache[dev][which] > 0) return cache[dev][which];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 76, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms() / 2;
+  }
+  if (dev >= 0 && dev < 64) cache[dev][which] = n;
+  return n;
 }
 
 }  // namespace tc
@@ -656,12 +791,13 @@ bool set_smem_attr() {
 cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
   using namespace tc;
   if (!set_smem_attr()) return cudaErrorInvalidConfiguration;
+  // boxes of 64 (K) x 128 rows: each CTA of a pair stages 128 rows of H and 128 of W
   CUtensorMap mH, mW;
-  if (!make_map(&mH, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mW, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, BK, BN)) return cudaErrorInvalidValue;
+  if (!make_map(&mH, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mW, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;
   FwdP p;
   p.r0 = a.r0; p.rows = a.rows; p.V = a.V;
-  p.mt = (a.rows + BM - 1) / BM;
+  p.mt = (a.rows + 255) / 256;
   p.ntn = (int)((a.V + BN - 1) / BN);
   p.kb = (int)((a.d + BK - 1) / BK);
   p.labels = a.labels;
@@ -669,9 +805,9 @@ cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
   p.part = a.part; p.ntiles = (a.V + kStatW - 1) / kStatW; p.zy = a.zy;
   p.status = a.status; p.limit_ns = wait_limit_ns();
   const int total = p.mt * p.ntn;
-  int grid = num_sms();
-  if (grid > total) grid = total;
-  k_fwd<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mH, mW, p);
+  int pairs = max_pairs((const void*)k_fwd);
+  if (pairs > total) pairs = total;
+  k_fwd<<<2 * pairs, NUM_THREADS, SMEM_BYTES, s>>>(mH, mW, p);
   return cudaGetLastError();
 }
 
@@ -680,26 +816,26 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   if (!set_smem_attr()) return cudaErrorInvalidConfiguration;
   CUtensorMap mGk, mGmn, mWmn, mHmn;
   // G: [rows, V] with row stride ldg; rows past the chunk read as zero.
-  if (!make_map(&mGk, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mGk, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, BK, 128)) return cudaErrorInvalidValue;
   if (!make_map(&mGmn, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mWmn, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mHmn, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
   BwdP p;
   p.rows = a.rows; p.r0 = a.r0; p.V = a.V; p.d = a.d;
-  p.mt_c = (a.rows + BM - 1) / BM;
+  p.mt_c = (a.rows + 255) / 256;
   p.nt_d = (int)((a.d + BN - 1) / BN);
   p.kb_v = (int)((a.V + BK - 1) / BK);
   p.splits = a.splits;
-  p.mt_v = (int)((a.V + BM - 1) / BM);
+  p.mt_v = (int)((a.V + 255) / 256);
   p.kb_c = (a.rows + BK - 1) / BK;
   p.n_dh = p.mt_c * p.nt_d * p.splits;
   p.n_total = p.n_dh + p.mt_v * p.nt_d;
   p.dh_part = a.dh_part; p.plane = (int64_t)a.rows * a.d;
   p.dW = a.dW; p.dw_acc = a.dw_accumulate;
   p.counter = a.counter; p.status = a.status; p.limit_ns = wait_limit_ns();
-  int grid = num_sms();
-  if (grid > p.n_total) grid = p.n_total;
-  k_bwd<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mGk, mGmn, mWmn, mHmn, p);
+  int pairs = max_pairs((const void*)k_bwd);
+  if (pairs > p.n_total) pairs = p.n_total;
+  k_bwd<<<2 * pairs, NUM_THREADS, SMEM_BYTES, s>>>(mGk, mGmn, mWmn, mHmn, p);
   return cudaGetLastError();
 }
 
