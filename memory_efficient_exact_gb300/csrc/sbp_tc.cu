@@ -215,7 +215,13 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t SMEM_BYTES = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+// k_bwd stages its dW output through shared memory: one 32x32 fp32 block (4 KB, 128-byte
+// swizzle) per epilogue warp, handed to the TMA unit for an asynchronous, coalesced
+// reduce-add (or store, first chunk) into dW.
+constexpr uint32_t STG_BYTES = 32 * 32 * 4;
+constexpr size_t SMEM_FWD = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+constexpr size_t SMEM_BWD = STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES + sizeof(Ctrl) + 1024;
+static_assert(SMEM_BWD <= 232448, "shared memory budget of one CTA");
 
 __device__ __forceinline__ uint32_t ctarank() {
   uint32_t r;
@@ -289,6 +295,26 @@ __device__ __forceinline__ void commit2_mc(uint64_t* bar, uint16_t mask) {
                    saddr(bar)),
                "h"(mask)
                : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void fail(Ctrl* c, int32_t* status) {
@@ -520,10 +546,12 @@ __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_bwd(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmGmn,
-               const __grid_constant__ CUtensorMap tmWmn, const __grid_constant__ CUtensorMap tmHmn, const BwdP p) {
+          const __grid_constant__ CUtensorMap tmWmn, const __grid_constant__ CUtensorMap tmHmn,
+          const __grid_constant__ CUtensorMap tmDW, const BwdP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  uint8_t* stg_base = base + STAGES * STAGE_BYTES;
+  Ctrl* c = reinterpret_cast<Ctrl*>(stg_base + NUM_EPI_WARPS * STG_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
   prologue(c, warp);
@@ -665,7 +693,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         vrow = row < p.V;
         dst = p.dW + row * p.d;
       }
-      const bool add = w.kind == 1 && p.dw_acc;
+      if (w.kind == 1) {
+        // dW rows [y0, y0+32) x columns [cg, cg+32): through the warp's staging block.
+        // Each dW element receives one add per launch (one unit owns each tile), so the
+        // TMA reduce-add is deterministic.  Rows past V and columns past d are clipped
+        // by the tensor map.
+        const uint32_t stg = saddr(stg_base + (warp - 2) * STG_BYTES);
+        const int y0 = w.mp * 256 + (int)rank * 128 + q * 32;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(tb + g * 32, r);
+          tmem_ld_wait();
+          const int64_t cg = c0 + g * 32;
+          if (cg >= p.d) continue;
+          if (lane == 0) bulk_wait_read();   // the previous block has left the staging buffer
+          __syncwarp();
+          // row `lane`, 16-byte chunk k stored at chunk k ^ (lane % 8): the 128-byte swizzle
+          // the tensor map reads, and conflict-free for the 32 lanes
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            sts128(stg + lane * 128 + ((k ^ (lane & 7)) << 4), r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0 && y0 < p.V) {
+            if (p.dw_acc) tma_reduce_add_2d(&tmDW, stg, (int)cg, y0);
+            else tma_store_2d(&tmDW, stg, (int)cg, y0);
+            bulk_commit();
+          }
+        }
+        release_tmem(c, buf, lane);
+        continue;
+      }
 #pragma unroll 1
       for (int g = 0; g < 4; ++g) {
         uint32_t r[32];
@@ -677,28 +737,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         float* o = dst + cg;
         if (cg + 32 <= p.d) {
           float4* o4 = reinterpret_cast<float4*>(o);
-          if (add) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              atomicAdd(o4 + k, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                            __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              o4[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                  __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-          }
+          for (int k = 0; k < 8; ++k)
+            o4[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (cg + j < p.d) {
-              if (add) atomicAdd(o + j, __uint_as_float(r[j]));
-              else o[j] = __uint_as_float(r[j]);
-            }
+            if (cg + j < p.d) o[j] = __uint_as_float(r[j]);
         }
       }
       release_tmem(c, buf, lane);
     }
+    if (lane == 0) bulk_wait_all();   // every dW block has left shared memory and landed
+    __syncwarp();
   }
   teardown(c, warp);
 }
@@ -721,6 +773,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // 2-D bf16 tensor map over a row-major [outer, inner] array with a row stride of
 // row_elems elements, 128-byte swizzle, zero fill outside the array.
+// 2-D fp32 tensor map for the dW output: [outer, inner] row-major, 32x32 boxes of
+// 128-byte rows, 128-byte swizzle.
+bool make_map_f32(CUtensorMap* m, void* ptr, uint64_t inner, uint64_t outer) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_elems, uint32_t box_in,
               uint32_t box_out) {
   auto enc = encoder();
@@ -750,8 +816,8 @@ bool set_smem_attr() {
   std::lock_guard<std::mutex> lk(mu);
   if (done == 0) {
     const bool ok =
-        cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) == cudaSuccess &&
-        cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) == cudaSuccess;
+        cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_FWD) == cudaSuccess &&
+        cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BWD) == cudaSuccess;
     done = ok ? 1 : -1;
   }
   return done == 1;
@@ -769,7 +835,7 @@ int max_pairs(const void* kernel) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 76, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = which == 0 ? SMEM_FWD : SMEM_BWD;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
@@ -807,7 +873,7 @@ cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
   const int total = p.mt * p.ntn;
   int pairs = max_pairs((const void*)k_fwd);
   if (pairs > total) pairs = total;
-  k_fwd<<<2 * pairs, NUM_THREADS, SMEM_BYTES, s>>>(mH, mW, p);
+  k_fwd<<<2 * pairs, NUM_THREADS, SMEM_FWD, s>>>(mH, mW, p);
   return cudaGetLastError();
 }
 
@@ -820,6 +886,8 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   if (!make_map(&mGmn, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mWmn, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mHmn, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  CUtensorMap mDW;
+  if (!make_map_f32(&mDW, a.dW, (uint64_t)a.d, (uint64_t)a.V)) return cudaErrorInvalidValue;
   BwdP p;
   p.rows = a.rows; p.r0 = a.r0; p.V = a.V; p.d = a.d;
   p.mt_c = (a.rows + 255) / 256;
@@ -835,7 +903,7 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   p.counter = a.counter; p.status = a.status; p.limit_ns = wait_limit_ns();
   int pairs = max_pairs((const void*)k_bwd);
   if (pairs > p.n_total) pairs = p.n_total;
-  k_bwd<<<2 * pairs, NUM_THREADS, SMEM_BYTES, s>>>(mGk, mGmn, mWmn, mHmn, p);
+  k_bwd<<<2 * pairs, NUM_THREADS, SMEM_BWD, s>>>(mGk, mGmn, mWmn, mHmn, mDW, p);
   return cudaGetLastError();
 }
 
