@@ -36,8 +36,9 @@ METRIC = "lm_head fwd+bwd tokens/s (SFT CE, d=4096, V=151936) and % BF16 tensor 
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # A small case of the same kernels for ncu captures: inputs larger than L2 (W 268 MB)
-# but about 1.5 GB on the device in total.
-PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T2048_d4096_V32768_chunk2048", objective="sft", T=2048,
+# but about 1.5 GB on the device in total; two chunks, so that the second launch of the
+# backward kernel accumulates into dW as every launch but the first of a call does.
+PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T4096_d4096_V32768_chunk2048", objective="sft", T=4096,
                         d=4096, V=32768, chunk=2048, dtype="bf16", seed=1002, mask="frac", frac=0.1)
 CPU_SAMPLE_TOKENS = 384
 
@@ -217,8 +218,33 @@ def run_ours(args):
     st = torch.zeros((), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        return sbp.sft(Ht, Wt, yt, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
+    objective = w.get("objective", "sft")
+    if objective == "grpo":
+        # per-response advantages; old log-probs near the workload's typical label
+        # log-prob (-log V) plus noise: their values steer only the clip branches
+        from memory_efficient_exact_gb300 import inputs as I
+        n_resp = max(1, T // 2048)
+        At = torch.from_numpy(I.make_advantages(n_resp, (T + n_resp - 1) // n_resp, w["seed"])[:T]).to(dev)
+        lpo = torch.from_numpy((-12.8 + I.make_logp_noise(T, w["seed"])).astype("float32")).to(dev)
+        ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_GRPO, dev)
+
+        def step():
+            return sbp.grpo(Ht, Wt, yt, At, lpo, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False,
+                            stream=stream)
+    elif objective == "dpo":
+        from memory_efficient_exact_gb300 import inputs as I
+        n_seq = max(2, T // 4096)
+        cu = torch.from_numpy(I.cu_seqlens(n_seq, T // n_seq)).to(dev)
+        sref = torch.from_numpy(I.make_ref_seq_logp(n_seq, w["seed"])).to(dev)
+        ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_DPO2, dev)
+
+        def step():
+            p1 = sbp.dpo_pass1(Ht, Wt, yt, cu, chunk, workspace=ws, status=st, logp=False, stream=stream)
+            return sbp.dpo_pass2(Ht, Wt, yt, cu, p1["seq_logp"], sref, 0.1, chunk, dH=dH, dW=dW, workspace=ws,
+                                 status=st, stream=stream)
+    else:
+        def step():
+            return sbp.sft(Ht, Wt, yt, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
 
     torch.cuda.reset_peak_memory_stats(dev)
     for _ in range(args.warmup):
@@ -226,6 +252,8 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     sbp.check_status(st, "warm-up")
     launches_per_call = sbp.last_launch_count()
+    if objective == "dpo":
+        launches_per_call *= 2   # (pass 2 and pass 1 enqueue the same number of launches)
 
     # ---- device-timed region: inputs resident in HBM (larger than L2: W is 1.24 GB) ----
     clocks = ClockSampler(gpu_id_for(torch, dev))
@@ -257,6 +285,7 @@ def run_ours(args):
     ms_per_step = ms / args.steps
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside ----
+    # (SFT call; for the other objectives the same copies wrap their step)
     Hh = torch.from_numpy(H).to(torch.bfloat16).pin_memory()
     yh = torch.from_numpy(y).pin_memory()
     dHh = torch.empty(Hh.shape, dtype=torch.bfloat16).pin_memory()
@@ -267,7 +296,11 @@ def run_ours(args):
     def e2e_step():
         Hd.copy_(Hh, non_blocking=True)
         yd.copy_(yh, non_blocking=True)
-        o = sbp.sft(Hd, Wt, yd, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
+        if objective == "sft":
+            o = sbp.sft(Hd, Wt, yd, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
+        else:
+            Ht.copy_(Hd)
+            o = step()
         dHh.copy_(o["dH"], non_blocking=True)
         lossh.copy_(o["loss"], non_blocking=True)
 
@@ -303,6 +336,8 @@ def run_ours(args):
     # of one chunk = 4 rows d V; the forward GEMM = 2 rows d V
     flops_bwd_launch = 4.0 * T * d * V / n_chunks
     flops_fwd_launch = 2.0 * T * d * V / n_chunks
+    # (DPO launches the forward twice per chunk, once per pass: the per-launch averages
+    # below divide by the launch counts, and the useful rate credits 6 d V per token)
     bwd_avg_s = bwd_ms / max(bwd_n, 1) / 1000.0
     fwd_avg_s = fwd_ms / max(fwd_n, 1) / 1000.0
     bwd_tf = flops_bwd_launch / bwd_avg_s / 1e12 if bwd_n else None
@@ -313,17 +348,18 @@ def run_ours(args):
     grad_gbs = gtb / (grad_ms / max(grad_n, 1) / 1000.0) if grad_n else None
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and objective == "sft":
         Ts = CPU_SAMPLE_TOKENS
         sec = cpu_oracle_sample(H, W, y, Ts)
         cpu = {"value": Ts / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"first {Ts} of the {T} tokens (full V={V}, d={d}), float64 numpy/BLAS, one run"}
 
+    metric = METRIC if objective == "sft" else f"lm_head fwd+bwd tokens/s ({objective}, d={d}, V={V})"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w["workload"], "objective": "sft", "T": T, "d": d, "V": V, "chunk": chunk,
+        "config": {"workload": w["workload"], "objective": objective, "T": T, "d": d, "V": V, "chunk": chunk,
                    "tokens_per_gpu_per_step": T, "ignored_frac": w["frac"],
                    "l2": f"inputs larger than L2 (W {V * d * 2 / 1e9:.2f} GB; chunk logits "
                          f"{chunk * V * 2 / 1e9:.2f} GB per chunk)",
@@ -374,16 +410,22 @@ def main(argv=None):
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
     ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
+    ap.add_argument("--objective", choices=["sft", "grpo", "dpo"], default="sft",
+                    help="grpo: 2048-token responses; dpo: 4096-token sequences, both passes per step")
     args = ap.parse_args(argv)
     if args.workload == "profile":
         WORKLOAD.clear()
         WORKLOAD.update(PROFILE_WORKLOAD)
         args.no_cpu_baseline = True
+    WORKLOAD["objective"] = args.objective
+    if args.objective == "dpo" and args.tokens is None and args.workload == "main":
+        WORKLOAD["T"] = 32768
     for key, val in (("chunk", args.chunk), ("T", args.tokens), ("d", args.d)):
         if val is not None:
             WORKLOAD[key] = val
-    if args.chunk is not None or args.tokens is not None or args.d is not None:
-        WORKLOAD["workload"] = (f"sft_ce_lmhead_bf16_T{WORKLOAD['T']}_d{WORKLOAD['d']}_V{WORKLOAD['V']}"
+    if args.chunk is not None or args.tokens is not None or args.d is not None or args.objective != "sft":
+        tag = {"sft": "sft_ce", "grpo": "grpo_clip", "dpo": "dpo_two_pass"}[args.objective]
+        WORKLOAD["workload"] = (f"{tag}_lmhead_bf16_T{WORKLOAD['T']}_d{WORKLOAD['d']}_V{WORKLOAD['V']}"
                                 f"_chunk{WORKLOAD['chunk']}")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

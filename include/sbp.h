@@ -106,6 +106,26 @@ int sbp_lmhead_grpo(const void* H, const void* W, const int32_t* labels,
                     void* dH, float* dW, int accumulate_dW,
                     void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* GRPO / PPO-clip variants on the same kernels: an optional KL penalty to a reference
+ * policy and an optional per-sequence mean (the ziziman.com article lists SFT, GRPO,
+ * PPO and DPO objectives; only the per-token weight changes).  Per-token term
+ *   l_t = -min(r_t A_t, clip(r_t, clip_lo, clip_hi) A_t) + kl_coef * KL_t,
+ *   KL_t = exp(q_t) - q_t - 1,  q_t = ref_logp_t - logp_t   (k3 estimator).
+ * cu_seqlens == NULL: L = token mean over the N non-ignored tokens (as sbp_lmhead_grpo).
+ * cu_seqlens != NULL (device int32 [n_seq+1], n_seq >= 1): L = (1/n_seq) sum_i of the
+ *   token mean of sequence i over its non-ignored tokens; a sequence without one
+ *   contributes 0; tokens outside every sequence get no weight.
+ * ref_logp: device fp32 [T], may be NULL when kl_coef == 0.  PPO-clip is this call
+ * with per-token advantages.  Other arguments as sbp_lmhead_grpo. */
+int sbp_lmhead_grpo_ext(const void* H, const void* W, const int32_t* labels,
+                        const float* advantages, const float* logp_old,
+                        float clip_lo, float clip_hi, const float* ref_logp, float kl_coef,
+                        const int32_t* cu_seqlens, int32_t n_seq,
+                        int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                        int dtype, float* loss, int64_t* n_valid, float* logp_out,
+                        void* dH, float* dW, int accumulate_dW,
+                        void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* DPO, first pass (ziziman.com article, DPO paragraph: the sigmoid couples the
  * positions, so the per-sequence sums are formed first).  Sequences are the token
  * ranges [cu_seqlens[i], cu_seqlens[i+1]), i < n_seq (cu_seqlens: device int32

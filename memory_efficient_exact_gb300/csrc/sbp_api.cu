@@ -173,9 +173,22 @@ struct CombineArgs {
   float* tokloss;          // [T] loss contribution of the token
   // GRPO
   const float* adv; const float* logp_old; float clip_lo, clip_hi;
-  // DPO pass 2
+  // DPO pass 2; GRPO per-sequence mean (seqw = each sequence's share of the mean)
   const int32_t* cu; int n_seq; const float* seqw;
+  // GRPO KL penalty
+  const float* ref_logp; float kl_coef;
 };
+
+// Index of the sequence holding token t (cu non-decreasing), or -1 outside all.
+__device__ __forceinline__ int seq_of(const int32_t* cu, int n_seq, int64_t t) {
+  if (n_seq <= 0 || t < cu[0] || t >= cu[n_seq]) return -1;
+  int lo = 0, hi = n_seq - 1;  // last i with cu[i] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 // One warp per row: lse = M + log sum_i s_i exp(m_i - M) over the row's tile partials,
 // logp = z_y - lse, then the objective's weight w and loss term.  The tile maxima are
@@ -214,18 +227,24 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
       const float rc = fminf(fmaxf(r, a.clip_lo), a.clip_hi);
       const float o = fminf(r * A, rc * A);
       const bool g = (A >= 0.f) ? (r <= a.clip_hi) : (r >= a.clip_lo);
-      w = g ? A * r * invN : 0.f;
-      tl = -o * invN;
+      float fac = invN;  // the token's share of the mean
+      if (a.cu) {
+        const int sq = seq_of(a.cu, a.n_seq, t);
+        fac = sq >= 0 ? a.seqw[sq] : 0.f;
+      }
+      float kl = 0.f, dkl = 0.f;  // k3 KL to the reference and its logp-derivative
+      if (a.ref_logp && a.kl_coef != 0.f) {
+        const float q = a.ref_logp[t] - logp;
+        const float eq = expf(q);
+        kl = eq - q - 1.f;
+        dkl = 1.f - eq;
+      }
+      w = fac * ((g ? A * r : 0.f) - a.kl_coef * dkl);
+      tl = fac * (-o + a.kl_coef * kl);
     }
   } else if (MODE == SBP_MODE_DPO2) {
-    if (valid && a.n_seq > 0 && t >= a.cu[0] && t < a.cu[a.n_seq]) {
-      int lo = 0, hi = a.n_seq - 1;  // last i with cu[i] <= t
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (a.cu[mid] <= t) lo = mid; else hi = mid - 1;
-      }
-      w = a.seqw[lo];
-    }
+    const int sq = valid ? seq_of(a.cu, a.n_seq, t) : -1;
+    if (sq >= 0) w = a.seqw[sq];
   }
   for (int64_t i = lane; i < a.ntiles; i += 32) p[i].x = w * expf(p[i].x - lse);
   if (lane == 0) {
@@ -361,6 +380,23 @@ __global__ void __launch_bounds__(256) k_seq_sums(const float* __restrict__ logp
   if (threadIdx.x == 0) seq_logp[i] = red[0];
 }
 
+// GRPO per-sequence mean: each sequence's share 1 / (n_seq * N_i) of the mean, N_i its
+// number of non-ignored tokens (0 when N_i = 0).  One block per sequence.
+__global__ void __launch_bounds__(256) k_seq_share(const int32_t* __restrict__ y, const int32_t* __restrict__ cu,
+                                                   int n_seq, int32_t ign, float* __restrict__ share) {
+  __shared__ int red[256];
+  const int i = blockIdx.x;
+  int c = 0;
+  for (int64_t t = cu[i] + threadIdx.x; t < cu[i + 1]; t += blockDim.x) c += y[t] != ign;
+  red[threadIdx.x] = c;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) share[i] = red[0] > 0 ? (float)(1.0 / ((double)n_seq * (double)red[0])) : 0.f;
+}
+
 __device__ __forceinline__ double softplus_d(double x) {
   return (x > 0 ? x : 0.0) + log1p(exp(-fabs(x)));
 }
@@ -408,6 +444,7 @@ struct Call {
   void* dH; float* dW; int accumulate_dW;
   // GRPO
   const float* adv; const float* logp_old; float clip_lo, clip_hi;
+  const float* ref_logp; float kl_coef;
   // DPO
   const int32_t* cu; int n_seq; double* seq_logp; const double* seq_in; const double* ref_in;
   float beta; double* margins;
@@ -432,6 +469,8 @@ int validate(const Call& c, Layout* L) {
   if (grad && c.T > 0 && !c.dH) return SBP_ERR_INVALID_ARG;
   if (c.mode == SBP_MODE_GRPO && c.T > 0 && (!c.adv || !c.logp_old)) return SBP_ERR_INVALID_ARG;
   if (c.mode == SBP_MODE_GRPO && !(c.clip_lo <= c.clip_hi)) return SBP_ERR_INVALID_ARG;
+  if (c.mode == SBP_MODE_GRPO && c.kl_coef != 0.f && c.T > 0 && !c.ref_logp) return SBP_ERR_INVALID_ARG;
+  if (c.mode == SBP_MODE_GRPO && c.cu && (c.n_seq < 1 || c.n_seq > L->max_seq)) return SBP_ERR_INVALID_ARG;
   if (c.mode == SBP_MODE_DPO1 || c.mode == SBP_MODE_DPO2) {
     if (c.n_seq < 0 || c.n_seq > L->max_seq || (c.n_seq > 0 && !c.cu)) return SBP_ERR_INVALID_ARG;
     if (c.mode == SBP_MODE_DPO1 && c.n_seq > 0 && !c.seq_logp) return SBP_ERR_INVALID_ARG;
@@ -476,6 +515,12 @@ int run(const Call& c) {
   SBP_CUDA(cudaGetLastError());
 
   const bool grad = c.mode != SBP_MODE_DPO1;
+  if (c.mode == SBP_MODE_GRPO && c.cu) {
+    prof::Scope ps(3, s);
+    k_seq_share<<<c.n_seq, 256, 0, s>>>(c.labels, c.cu, c.n_seq, c.ign, seqw);
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+  }
   if (c.mode == SBP_MODE_DPO2) {
     k_dpo_scales<<<1, 32, 0, s>>>(c.seq_in, c.ref_in, c.n_seq, (double)c.beta, c.loss, c.margins, seqw);
     ++launches;
@@ -514,6 +559,7 @@ int run(const Call& c) {
     ca.V = c.V; ca.ign = c.ign; ca.nvalid = nvalid; ca.w_row = w_row; ca.logp = logp; ca.tokloss = tokloss;
     ca.adv = c.adv; ca.logp_old = c.logp_old; ca.clip_lo = c.clip_lo; ca.clip_hi = c.clip_hi;
     ca.cu = c.cu; ca.n_seq = c.n_seq; ca.seqw = seqw;
+    ca.ref_logp = c.ref_logp; ca.kl_coef = c.kl_coef;
     const unsigned gc = (unsigned)((rows + 7) / 8);
     {
     prof::Scope ps(3, s);
@@ -656,6 +702,23 @@ int sbp_lmhead_grpo(const void* H, const void* W, const int32_t* labels, const f
   c.dH = dH; c.dW = dW; c.accumulate_dW = accumulate_dW; c.adv = advantages; c.logp_old = logp_old;
   c.clip_lo = clip_lo; c.clip_hi = clip_hi; c.ws = workspace; c.ws_bytes = ws_bytes;
   c.dev_status = dev_status; c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int sbp_lmhead_grpo_ext(const void* H, const void* W, const int32_t* labels, const float* advantages,
+                        const float* logp_old, float clip_lo, float clip_hi, const float* ref_logp, float kl_coef,
+                        const int32_t* cu_seqlens, int32_t n_seq, int64_t T, int64_t d, int64_t V, int64_t chunk,
+                        int32_t ignore_index, int dtype, float* loss, int64_t* n_valid, float* logp_out, void* dH,
+                        float* dW, int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                        void* stream) {
+  if (!loss) return SBP_ERR_INVALID_ARG;
+  Call c{};
+  c.mode = SBP_MODE_GRPO; c.H = H; c.W = W; c.labels = labels; c.T = T; c.d = d; c.V = V; c.chunk = chunk;
+  c.ign = ignore_index; c.dtype = dtype; c.loss = loss; c.n_valid = n_valid; c.logp_out = logp_out;
+  c.dH = dH; c.dW = dW; c.accumulate_dW = accumulate_dW; c.adv = advantages; c.logp_old = logp_old;
+  c.clip_lo = clip_lo; c.clip_hi = clip_hi; c.ref_logp = ref_logp; c.kl_coef = kl_coef;
+  c.cu = cu_seqlens; c.n_seq = cu_seqlens ? n_seq : 0;
+  c.ws = workspace; c.ws_bytes = ws_bytes; c.dev_status = dev_status; c.stream = static_cast<cudaStream_t>(stream);
   return run(c);
 }
 

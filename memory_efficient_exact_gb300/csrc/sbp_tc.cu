@@ -466,48 +466,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
       const int64_t c0 = (int64_t)nb * BN + h * 128;
-      float m = -INFINITY, zyv = 0.f;
-      bool has_y = false;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tb + g * 32, r);
-        tmem_ld_wait();
-        const int64_t cg = c0 + g * 32;
+      // the row's 128 accumulator columns of this half tile, then the buffer goes back
+      // to the MMA at once: the statistics below run while the next tile accumulates
+      uint32_t r[4][32];
+      __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float v = __uint_as_float(r[j]);
-          if (cg + j < p.V) m = fmaxf(m, v);
-          if (cg + j == (int64_t)y) { zyv = v; has_y = true; }
-        }
+      for (int g = 0; g < 4; ++g) tmem_ld32(tb + g * 32, r[g]);
+      tmem_ld_wait();
+      release_tmem(c, buf, lane);
+      const int64_t nv = p.V - c0;                  // valid columns of this half tile
+      const int ncol = nv >= 128 ? 128 : (nv > 0 ? (int)nv : 0);
+      float m = -INFINITY;
+      if (ncol == 128) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m = fmaxf(m, __uint_as_float(r[g][j]));
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (g * 32 + j < ncol) m = fmaxf(m, __uint_as_float(r[g][j]));
+      }
+      const int64_t jy = (int64_t)y - c0;           // the label's column within the half tile
+      const bool has_y = vrow && jy >= 0 && jy < ncol;
+      float zyv = 0.f;
+      if (has_y) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (g * 32 + j == (int)jy) zyv = __uint_as_float(r[g][j]);
       }
       const float mb2 = m * L2E;
       float s = 0.f;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tb + g * 32, r);
-        tmem_ld_wait();
-        const int64_t cg = c0 + g * 32;
-        if (cg >= p.V) continue;
-        uint32_t hv[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float e0 = (cg + j < p.V) ? ex2(fmaf(__uint_as_float(r[j]), L2E, -mb2)) : 0.f;
-          const float e1 = (cg + j + 1 < p.V) ? ex2(fmaf(__uint_as_float(r[j + 1]), L2E, -mb2)) : 0.f;
-          s += e0 + e1;
-          const __half2 hh = __floats2half2_rn(e0, e1);
-          hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+      for (int g = 0; g < 4; ++g) {
+        if (g * 32 >= ncol) break;
+        uint32_t hv[16];
+        if (ncol == 128) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float e0 = ex2(fmaf(__uint_as_float(r[g][j]), L2E, -mb2));
+            const float e1 = ex2(fmaf(__uint_as_float(r[g][j + 1]), L2E, -mb2));
+            s += e0 + e1;
+            const __half2 hh = __floats2half2_rn(e0, e1);
+            hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float e0 = (g * 32 + j < ncol) ? ex2(fmaf(__uint_as_float(r[g][j]), L2E, -mb2)) : 0.f;
+            const float e1 = (g * 32 + j + 1 < ncol) ? ex2(fmaf(__uint_as_float(r[g][j + 1]), L2E, -mb2)) : 0.f;
+            s += e0 + e1;
+            const __half2 hh = __floats2half2_rn(e0, e1);
+            hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
         }
         if (p.E && vrow) {
-          uint4* dst = reinterpret_cast<uint4*>(p.E + (int64_t)row * p.lde + cg);
+          uint4* dst = reinterpret_cast<uint4*>(p.E + (int64_t)row * p.lde + c0 + g * 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) dst[k] = make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
         }
       }
-      release_tmem(c, buf, lane);
       const int64_t tix = (int64_t)nb * 2 + h;
       if (vrow && tix < p.ntiles) p.part[(int64_t)row * p.ntiles + tix] = make_float2(m, s);
       if (vrow && has_y) p.zy[row] = zyv;
@@ -693,6 +715,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         vrow = row < p.V;
         dst = p.dW + row * p.d;
       }
+      uint32_t r[4][32];
+      __syncwarp();
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tmem_ld32(tb + g * 32, r[g]);
+      tmem_ld_wait();
+      release_tmem(c, buf, lane);
       if (w.kind == 1) {
         // dW rows [y0, y0+32) x columns [cg, cg+32): through the warp's staging block.
         // Each dW element receives one add per launch (one unit owns each tile), so the
@@ -700,21 +728,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // by the tensor map.
         const uint32_t stg = saddr(stg_base + (warp - 2) * STG_BYTES);
         const int y0 = w.mp * 256 + (int)rank * 128 + q * 32;
-#pragma unroll 1
+#pragma unroll
         for (int g = 0; g < 4; ++g) {
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld32(tb + g * 32, r);
-          tmem_ld_wait();
           const int64_t cg = c0 + g * 32;
-          if (cg >= p.d) continue;
+          if (cg >= p.d) break;
           if (lane == 0) bulk_wait_read();   // the previous block has left the staging buffer
           __syncwarp();
           // row `lane`, 16-byte chunk k stored at chunk k ^ (lane % 8): the 128-byte swizzle
           // the tensor map reads, and conflict-free for the 32 lanes
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            sts128(stg + lane * 128 + ((k ^ (lane & 7)) << 4), r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+            sts128(stg + lane * 128 + ((k ^ (lane & 7)) << 4), r[g][4 * k], r[g][4 * k + 1], r[g][4 * k + 2],
+                   r[g][4 * k + 3]);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0 && y0 < p.V) {
@@ -723,31 +748,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bulk_commit();
           }
         }
-        release_tmem(c, buf, lane);
         continue;
       }
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tb + g * 32, r);
-        tmem_ld_wait();
-        const int64_t cg = c0 + g * 32;
-        if (!vrow || cg >= p.d) continue;
-        float* o = dst + cg;
-        if (cg + 32 <= p.d) {
-          float4* o4 = reinterpret_cast<float4*>(o);
+      if (vrow) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            o4[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-        } else {
+        for (int g = 0; g < 4; ++g) {
+          const int64_t cg = c0 + g * 32;
+          if (cg >= p.d) break;
+          float* o = dst + cg;
+          if (cg + 32 <= p.d) {
+            float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (cg + j < p.d) o[j] = __uint_as_float(r[j]);
+            for (int k = 0; k < 8; ++k)
+              o4[k] = make_float4(__uint_as_float(r[g][4 * k]), __uint_as_float(r[g][4 * k + 1]),
+                                  __uint_as_float(r[g][4 * k + 2]), __uint_as_float(r[g][4 * k + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (cg + j < p.d) o[j] = __uint_as_float(r[g][j]);
+          }
         }
       }
-      release_tmem(c, buf, lane);
     }
     if (lane == 0) bulk_wait_all();   // every dW block has left shared memory and landed
     __syncwarp();

@@ -45,6 +45,9 @@ def _load() -> ctypes.CDLL:
     lib.sbp_lmhead_sft.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, SZ, P, P]
     lib.sbp_lmhead_grpo.restype = C
     lib.sbp_lmhead_grpo.argtypes = [P, P, P, P, P, F, F, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, SZ, P, P]
+    lib.sbp_lmhead_grpo_ext.restype = C
+    lib.sbp_lmhead_grpo_ext.argtypes = [P, P, P, P, P, F, F, P, F, P, I32, I64, I64, I64, I64, I32, C, P, P, P, P, P,
+                                        C, P, SZ, P, P]
     lib.sbp_lmhead_dpo_pass1.restype = C
     lib.sbp_lmhead_dpo_pass1.argtypes = [P, P, P, P, I32, I64, I64, I64, I64, I32, C, P, P, P, P, SZ, P, P]
     lib.sbp_lmhead_dpo_pass2.restype = C
@@ -220,6 +223,31 @@ def grpo(H, W, labels, advantages, logp_old, chunk, clip_lo=0.8, clip_hi=1.2, ig
                                 chunk, ignore_index, dt, _p(loss), _p(nv), _p(lp), _p(dH), _p(dW),
                                 int(bool(accumulate_dW)), _p(ws), ws.numel(), _p(st), _stream(stream)),
            "sbp_lmhead_grpo")
+    return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
+
+
+def grpo_ext(H, W, labels, advantages, logp_old, chunk, clip_lo=0.8, clip_hi=1.2, ref_logp=None, kl_coef=0.0,
+             cu_seqlens=None, ignore_index=IGNORE_INDEX, *, dH=None, dW=None, accumulate_dW=False, logp=True,
+             workspace=None, status=None, stream=None) -> dict:
+    """GRPO / PPO-clip with an optional KL penalty and per-sequence mean (``sbp_lmhead_grpo_ext``)."""
+    T, d, V, dt, ws = _prep(H, W, labels, chunk, MODE_GRPO, workspace)
+    _dev(advantages, logp_old, ref_logp, cu_seqlens)
+    if advantages.dtype != torch.float32 or logp_old.dtype != torch.float32:
+        raise TypeError("advantages and logp_old must be float32")
+    if ref_logp is not None and ref_logp.dtype != torch.float32:
+        raise TypeError("ref_logp must be float32")
+    n_seq = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dH, dW = _grad_out(H, W, dH, dW)
+    dev = H.device
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    nv = torch.empty((), dtype=torch.int64, device=dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev) if logp else None
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_lmhead_grpo_ext(_p(H), _p(W), _p(labels), _p(advantages), _p(logp_old), clip_lo, clip_hi,
+                                    _p(ref_logp), float(kl_coef), _p(cu_seqlens), n_seq, T, d, V, chunk,
+                                    ignore_index, dt, _p(loss), _p(nv), _p(lp), _p(dH), _p(dW),
+                                    int(bool(accumulate_dW)), _p(ws), ws.numel(), _p(st), _stream(stream)),
+           "sbp_lmhead_grpo_ext")
     return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
 
 

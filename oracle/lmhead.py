@@ -144,6 +144,55 @@ def grpo(H, W, y, advantages, logp_old, ignore_index: int = IGNORE_INDEX,
     return dict(loss=loss, n_valid=N, logp=f["logp"], lse=f["lse"], G=G, dH=dH, dW=dW)
 
 
+def kl_k3(logp, ref_logp):
+    """Per-token KL estimate to a reference policy, k3 form: exp(q) - q - 1 with
+    q = ref_logp - logp (non-negative, zero when the two agree)."""
+    q = _f64(ref_logp) - _f64(logp)
+    return np.exp(q) - q - 1.0
+
+
+def grpo_ext(H, W, y, advantages, logp_old, ignore_index: int = IGNORE_INDEX, clip_lo: float = 0.8,
+             clip_hi: float = 1.2, ref_logp=None, kl_coef: float = 0.0, cu_seqlens=None) -> dict:
+    """GRPO / PPO-clip with an optional KL penalty and an optional per-sequence mean.
+
+    Per-token term  l_t = -min(r_t A_t, clip(r_t) A_t) + kl_coef * KL_t,
+    KL_t = exp(q_t) - q_t - 1, q_t = ref_logp_t - logp_t (k3 estimator).
+    Reduction (reading): with cu_seqlens None, the token mean over the N non-ignored
+    tokens; otherwise the mean over the S sequences of each sequence's token mean,
+    L = (1/S) sum_i (1/N_i) sum_{t in i, valid} l_t, where a sequence without a valid
+    token contributes 0 (and still counts in S); tokens outside every sequence get no
+    weight.  dl_t/dlogp_t = -g_t A_t r_t + kl_coef (1 - exp(q_t)), so the logit-gradient
+    weight is w_t = f_t (g_t A_t r_t - kl_coef (1 - exp(q_t))) with f_t the token's
+    share of the mean.
+    """
+    f = forward(H, W, y, ignore_index)
+    T = f["P"].shape[0]
+    valid = f["valid"]
+    o, gar = grpo_weight(f["logp"], logp_old, advantages, valid, clip_lo, clip_hi)
+    if ref_logp is not None and kl_coef != 0.0:
+        kl = np.where(valid, kl_k3(f["logp"], ref_logp), 0.0)
+        dkl = np.where(valid, 1.0 - np.exp(_f64(ref_logp) - f["logp"]), 0.0)
+    else:
+        kl = np.zeros(T)
+        dkl = np.zeros(T)
+    term = np.where(valid, -o + kl_coef * kl, 0.0)
+    if cu_seqlens is None:
+        N = f["n_valid"]
+        fac = np.where(valid, 1.0 / N if N else 0.0, 0.0)
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        S = len(cu) - 1
+        sid = seq_index(cu, T)
+        Ni = np.array([int(valid[cu[i]:cu[i + 1]].sum()) for i in range(S)])
+        per = np.where(Ni > 0, 1.0 / (S * np.maximum(Ni, 1)), 0.0)
+        fac = np.where(valid & (sid >= 0), per[np.maximum(sid, 0)] if S else 0.0, 0.0)
+    loss = float((term * fac).sum())
+    w = fac * (gar - kl_coef * dkl)
+    G = _logit_grad(f, w)
+    dH, dW = _backward(G, H, W)
+    return dict(loss=loss, n_valid=f["n_valid"], logp=f["logp"], lse=f["lse"], G=G, dH=dH, dW=dW, weight=w)
+
+
 def seq_index(cu_seqlens, T: int) -> np.ndarray:
     """Sequence id of every token; tokens outside [cu[0], cu[-1]) get -1."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)

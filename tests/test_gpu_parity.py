@@ -94,6 +94,36 @@ def test_grpo_parity(sbp, dtype, T, d, V, chunk):
     check_grads(dtype, out, ref, y)
 
 
+@pytest.mark.parametrize("dtype,T,d,V,chunk,per_seq,kl", [("fp32", 64, 32, 200, 16, True, 0.3),
+                                                            ("bf16", 300, 256, 2000, 128, True, 0.1),
+                                                            ("bf16", 520, 128, 1000, 256, False, 0.5)])
+def test_grpo_variants_parity(sbp, dtype, T, d, V, chunk, per_seq, kl):
+    H, W, y = make_case(T, d, V, dtype, seed=17 + T, w_std=0.1)
+    f = O.forward(H, W, y, IGN)
+    lens = [T // 4, T // 3, T // 6, T - (T // 4 + T // 3 + T // 6)]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    A = I.make_advantages(len(lens), T, seed=T)[:T].astype(np.float32)
+    lpo = (f["logp"] + I.make_logp_noise(T, seed=T)).astype(np.float32)
+    ref = (f["logp"] + 0.3 * I.make_logp_noise(T, seed=T + 1)).astype(np.float32)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    At, lpot, reft = (torch.from_numpy(x).cuda() for x in (A, lpo, ref))
+    cut = torch.from_numpy(cu).cuda() if per_seq else None
+    out = sbp.grpo_ext(Ht, Wt, yt, At, lpot, chunk, ref_logp=reft, kl_coef=kl, cu_seqlens=cut)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    refo = O.grpo_ext(H, W, y, A.astype(np.float64), lpo.astype(np.float64), IGN, ref_logp=ref.astype(np.float64),
+                      kl_coef=kl, cu_seqlens=cu if per_seq else None)
+    tol = TOL[dtype]
+    assert int(out["n_valid"].item()) == refo["n_valid"]
+    assert rel(out["loss"].item(), refo["loss"]) <= tol["loss"], (out["loss"].item(), refo["loss"])
+    check_grads(dtype, out, refo, y)
+    # without the extras the variant is the plain GRPO call, bit for bit
+    a = sbp.grpo_ext(Ht, Wt, yt, At, lpot, chunk)
+    b = sbp.grpo(Ht, Wt, yt, At, lpot, chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(a["dH"], b["dH"]) and torch.equal(a["dW"], b["dW"]) and torch.equal(a["loss"], b["loss"])
+
+
 @pytest.mark.parametrize("dtype,lens,d,V,chunk", [("fp32", [30, 20, 25, 21], 32, 200, 40),
                                                    ("bf16", [200, 96, 150, 74], 256, 2000, 128),
                                                    ("bf16", [128, 256, 64, 192, 100, 100], 128, 1024, 100)])

@@ -368,3 +368,62 @@ def test_planted_per_chunk_mean_is_caught():
         s = L.sft(H[r0:r0 + 4], W, y[r0:r0 + 4], IGN)
         dH[r0:r0 + 4] = s["dH"]
     assert rel(dH, ref["dH"]) > 1e-3
+
+
+# ----------------------------------------------------------------------------- GRPO variants
+
+def _ext_inputs(seed=30):
+    H, W, y, A, lpo = _grpo_inputs(seed)
+    f = L.forward(H, W, y, IGN)
+    ref = f["logp"] + np.array([0.3, -0.2, 0.5, -0.4, 0.1, 0.25])
+    return H, W, y, A, lpo, ref
+
+
+@pytest.mark.parametrize("cu", [None, np.array([0, 2, 6])])
+def test_fd_grpo_with_kl_and_reduction(cu):
+    H, W, y, A, lpo, ref = _ext_inputs()
+    _fd_check(lambda: L.grpo_ext(H, W, y, A, lpo, IGN, ref_logp=ref, kl_coef=0.7, cu_seqlens=cu), H, W)
+
+
+def test_grpo_ext_reduces_to_grpo():
+    H, W, y, A, lpo, ref = _ext_inputs(31)
+    a = L.grpo(H, W, y, A, lpo, IGN)
+    b = L.grpo_ext(H, W, y, A, lpo, IGN)
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-14)
+    np.testing.assert_allclose(b["dH"], a["dH"], rtol=1e-13, atol=1e-17)
+    np.testing.assert_allclose(b["dW"], a["dW"], rtol=1e-13, atol=1e-17)
+
+
+def test_kl_term_vanishes_at_the_reference():
+    H, W, y, A, lpo, _ = _ext_inputs(32)
+    f = L.forward(H, W, y, IGN)
+    a = L.grpo(H, W, y, A, lpo, IGN)
+    b = L.grpo_ext(H, W, y, A, lpo, IGN, ref_logp=f["logp"], kl_coef=3.0)
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-12)
+    np.testing.assert_allclose(b["dH"], a["dH"], rtol=1e-11, atol=1e-15)
+    # k3 is non-negative and second order in q
+    q = np.linspace(-2, 2, 41)
+    k = L.kl_k3(np.zeros_like(q), q)
+    assert np.all(k >= 0) and abs(L.kl_k3(0.0, 1e-4) - 0.5e-8) < 1e-12
+
+
+def test_sequence_mean_equals_token_mean_for_equal_counts():
+    H, W, y = tiny(T=12, d=4, V=6, seed=33, n_ignore=0)
+    A = np.random.default_rng(1).standard_normal(12)
+    lpo = L.forward(H, W, y, IGN)["logp"] + 0.05
+    cu = np.array([0, 4, 8, 12])
+    a = L.grpo_ext(H, W, y, A, lpo, IGN)
+    b = L.grpo_ext(H, W, y, A, lpo, IGN, cu_seqlens=cu)
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-13)
+    np.testing.assert_allclose(b["dW"], a["dW"], rtol=1e-12, atol=1e-17)
+    # with unequal counts the two reductions differ
+    c = L.grpo_ext(H, W, y, A, lpo, IGN, cu_seqlens=np.array([0, 2, 12]))
+    assert abs(c["loss"] - a["loss"]) > 1e-6
+
+
+def test_planted_kl_sign_is_caught(monkeypatch):
+    real = L.kl_k3
+    monkeypatch.setattr(L, "kl_k3", lambda lp, ref: -real(lp, ref))
+    H, W, y, A, lpo, ref = _ext_inputs()
+    with pytest.raises(AssertionError):
+        _fd_check(lambda: L.grpo_ext(H, W, y, A, lpo, IGN, ref_logp=ref, kl_coef=0.7), H, W)
