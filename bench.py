@@ -3,9 +3,9 @@
 
 Workload: SFT cross-entropy forward + backward of the LM head through the C ABI
 (``sbp_lmhead_sft``), bf16 operands with fp32 accumulation, T = 16384 tokens
-(8 x 2048), d = 4096, V = 151936, chunk = 2048; H ~ N(0,1), W ~ N(0, 0.02^2),
+(8 x 2048), d = 4096, V = 151936, chunk = 4096; H ~ N(0,1), W ~ N(0, 0.02^2),
 labels uniform with 10% ignored -- synthetic, Qwen3-shaped.  One step = one call =
-the whole hot path (label scan, 8 x [forward GEMM + statistics, combine, logit
+the whole hot path (label scan, 4 x [forward GEMM + statistics, combine, logit
 gradient, dH/dW GEMMs, dH reduce], loss reduction) over one batch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -30,17 +30,22 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T16384_d4096_V151936_chunk2048", objective="sft", T=16384, d=4096,
-                V=151936, chunk=2048, dtype="bf16", seed=1002, mask="frac", frac=0.1)
+WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T16384_d4096_V151936_chunk4096", objective="sft", T=16384, d=4096,
+                V=151936, chunk=4096, dtype="bf16", seed=1002, mask="frac", frac=0.1)
 METRIC = "lm_head fwd+bwd tokens/s (SFT CE, d=4096, V=151936) and % BF16 tensor peak"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# A small case of the same kernels for ncu captures: inputs larger than L2 (W 268 MB)
-# but about 1.5 GB on the device in total; two chunks, so that the second launch of the
+# A small case of the same kernels for ncu captures: the bench's chunk and d, V = 32768
+# (W 268 MB, larger than L2), about 1.6 GB on the device in total; two chunks, so that the second launch of the
 # backward kernel accumulates into dW as every launch but the first of a call does.
-PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T4096_d4096_V32768_chunk2048", objective="sft", T=4096,
-                        d=4096, V=32768, chunk=2048, dtype="bf16", seed=1002, mask="frac", frac=0.1)
+PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T8192_d4096_V32768_chunk4096", objective="sft", T=8192,
+                        d=4096, V=32768, chunk=4096, dtype="bf16", seed=1002, mask="frac", frac=0.1)
 CPU_SAMPLE_TOKENS = 384
+# DRAM bytes (read + write) of one accumulating k_bwd launch, from an ncu capture of the
+# profile workload (d = 4096, chunk 4096, V = 32768: 2.444 GB read + 0.566 GB written),
+# scaled to V = 151936 by the units processed (every operand but H_c grows with V).  Only
+# valid for the main workload's shape and the kernel version it was captured on.
+K_BWD_TRAFFIC_BYTES = (2.444e9 + 0.566e9) * 151936 / 32768
 
 
 def load_peaks():
@@ -366,7 +371,9 @@ def run_ours(args):
                    "parallelism": f"dp{world} replicas (no collective)"},
         "roofline": {"kernel": "k_bwd (dH and dW GEMMs of one chunk)", "bound": "tensor",
                      "achieved": bwd_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": (bwd_tf / peak_tf) if bwd_tf else None, "traffic": None,
+                     "frac": (bwd_tf / peak_tf) if bwd_tf else None,
+                     "traffic": K_BWD_TRAFFIC_BYTES if (d, V, chunk) == (4096, 151936, 4096) and
+                     objective == "sft" else None,
                      "peak_source": f"bf16 dense, sustained, {peak_src}",
                      "algorithmic_flops_per_launch": flops_bwd_launch, "launches": bwd_n,
                      "avg_launch_ms": bwd_avg_s * 1e3},

@@ -166,6 +166,26 @@ int sbp_lmhead_dpo_pass2(const void* H, const void* W, const int32_t* labels,
 int sbp_profile_enable(int on);
 int sbp_profile_read(double* ms, int64_t* launches, int n);
 
+/* Chunked exact backward of a position-wise SwiGLU MLP sublayer (the layer below the LM
+ * head; StreamBP decomposes the chain rule along the sequence layer by layer: the
+ * chatpaper.ai / fugumt.com abstract and the atlas.scime.ai "Approach").  With x the
+ * sublayer's (normalised) input,
+ *     g = x Wg^T,  u = x Wu^T,  a = silu(g) * u,  y = a Wd^T,
+ * and dY = dL/dy, every chunk of `chunk` rows recomputes its g, u, a and forms
+ *     da = dY Wd, dg = da * u * silu'(g), du = da * silu(g),
+ *     dX = dg Wg + du Wu,  dWd (+)= dY^T a,  [dWg; dWu] (+)= [dg du]^T x,
+ * so no [T, f] activation exists beyond one chunk.  bf16 operands, fp32 accumulation.
+ *   X, dY  [T, d] bf16;  Wgu [2f, d] bf16 = Wg (rows 0..f-1) then Wu (rows f..2f-1);
+ *   Wd [d, f] bf16;  dX [T, d] bf16 (overwritten);  dWgu [2f, d] fp32, dWd [d, f] fp32
+ *   (overwritten when accumulate = 0, added to when 1).
+ * d must be a multiple of 64 and f of 256.  Workspace, stream and error rules as for the
+ * LM-head calls. */
+size_t sbp_mlp_workspace_bytes(int64_t T, int64_t d, int64_t f, int64_t chunk);
+int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, const void* dY,
+                            int64_t T, int64_t d, int64_t f, int64_t chunk,
+                            void* dX, float* dWgu, float* dWd, int accumulate,
+                            void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Size of the fixed scratch array that sbp_lmhead_sft_noalloc works in (bytes). */
 #define SBP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -636,6 +637,100 @@ int run(const Call& c) {
   return SBP_OK;
 }
 
+// ------------------------------------------------------------------------- MLP sublayer
+
+struct MlpLayout {
+  int64_t chunk = 0, n_chunks = 0;
+  int splits = 1;
+  size_t off_gu = 0, off_a = 0, off_dhp = 0, off_cnt = 0, total = 0;
+};
+
+bool mlp_layout(int64_t T, int64_t d, int64_t f, int64_t chunk, MlpLayout* L) {
+  if (T < 0 || d < 64 || f < 256 || d % 64 || f % 256 || chunk < 1 || chunk > 65535) return false;
+  MlpLayout l;
+  l.chunk = T > 0 ? (chunk < T ? chunk : T) : 1;
+  l.n_chunks = T > 0 ? (T + l.chunk - 1) / l.chunk : 0;
+  l.splits = choose_splits(l.chunk, d, 2 * f, num_sms());
+  size_t o = 0;
+  l.off_gu = o;  o = align256(o + (size_t)l.chunk * 2 * f * 2);
+  l.off_a = o;   o = align256(o + (size_t)l.chunk * f * 2);
+  l.off_dhp = o; o = align256(o + (size_t)l.splits * l.chunk * d * sizeof(float));
+  l.off_cnt = o; o = align256(o + (size_t)(2 * l.n_chunks + 1) * sizeof(uint32_t));
+  l.total = o;
+  *L = l;
+  return true;
+}
+
+int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int64_t T, int64_t d, int64_t f,
+            int64_t chunk, void* dX, float* dWgu, float* dWd, int accumulate, void* ws, size_t ws_bytes,
+            int32_t* dev_status, cudaStream_t s) {
+  MlpLayout L;
+  if (!mlp_layout(T, d, f, chunk, &L)) return SBP_ERR_INVALID_ARG;
+  if (!Wgu || !Wd || !dWgu || !dWd || !dev_status) return SBP_ERR_INVALID_ARG;
+  if (T > 0 && (!X || !dY || !dX)) return SBP_ERR_INVALID_ARG;
+  if (T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
+  for (const void* q : {X, Wgu, Wd, dY, (const void*)dX, (const void*)dWgu, (const void*)dWd})
+    if (q && !al16(q)) return SBP_ERR_ALIGNMENT;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return SBP_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  void* gu = w + L.off_gu;
+  void* abuf = w + L.off_a;
+  float* dhp = reinterpret_cast<float*>(w + L.off_dhp);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(w + L.off_cnt);
+  int launches = 0;
+  SBP_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
+  SBP_CUDA(cudaMemsetAsync(cnt, 0, (size_t)(2 * L.n_chunks + 1) * sizeof(uint32_t), s));
+  if (T == 0 && !accumulate) {
+    k_zero_f32<<<grid_for(2 * f * d, 256), 256, 0, s>>>(dWgu, 2 * f * d);
+    k_zero_f32<<<grid_for(d * f, 256), 256, 0, s>>>(dWd, d * f);
+    launches += 2;
+    SBP_CUDA(cudaGetLastError());
+  }
+  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+    const int64_t r0 = ci * L.chunk;
+    const int rows = (int)((r0 + L.chunk <= T) ? L.chunk : T - r0);
+    const int acc = (ci > 0 || accumulate) ? 1 : 0;
+    {
+      // recompute g, u and a = silu(g) u for the chunk, then dg | du in place
+      prof::Scope ps(0, s);
+      TcMlpArgs m{};
+      m.Arows = X; m.T = T; m.d = d; m.f = f; m.B = Wgu; m.r0 = r0; m.rows = rows; m.Aout = abuf; m.GU = gu;
+      m.status = dev_status;
+      SBP_CUDA(tc_mlp(m, false, s));
+      m.Arows = dY; m.B = Wd;
+      SBP_CUDA(tc_mlp(m, true, s));
+      launches += 2;
+    }
+    const int splits = std::min(choose_splits(rows, d, 2 * f, num_sms()), L.splits);
+    {
+      // dX_c = [dg du] [Wg; Wu] and [dWg; dWu] (+)= [dg du]^T x_c
+      prof::Scope ps(1, s);
+      TcBwdArgs b{};
+      b.G = gu; b.ldg = 2 * f; b.H = X; b.W = Wgu; b.T = T; b.d = d; b.V = 2 * f; b.r0 = r0; b.rows = rows;
+      b.splits = splits; b.dh_part = dhp; b.dW = dWgu; b.dw_accumulate = acc; b.counter = cnt + 2 * ci;
+      b.status = dev_status;
+      SBP_CUDA(tc_backward(b, s));
+      // dWd (+)= dY_c^T a_c : the dW units only, with M over d and N over f
+      TcBwdArgs e{};
+      e.G = static_cast<const __nv_bfloat16*>(dY) + r0 * d; e.ldg = d; e.H = abuf; e.W = Wd; e.T = rows;
+      e.d = f; e.V = d; e.r0 = 0; e.rows = rows; e.splits = 1; e.dh_part = dhp; e.dW = dWd;
+      e.dw_accumulate = acc; e.counter = cnt + 2 * ci + 1; e.status = dev_status; e.dw_only = 1;
+      SBP_CUDA(tc_backward(e, s));
+      launches += 2;
+    }
+    {
+      prof::Scope ps(3, s);
+      const int64_t n = (int64_t)rows * d;
+      k_dh_reduce<__nv_bfloat16><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
+          dhp, splits, n, n, static_cast<__nv_bfloat16*>(dX) + r0 * d);
+      ++launches;
+      SBP_CUDA(cudaGetLastError());
+    }
+  }
+  g_launches = launches;
+  return SBP_OK;
+}
+
 }  // namespace
 
 // Scratch of sbp_lmhead_sft_noalloc: a fixed device array in this module, so that
@@ -767,6 +862,19 @@ int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels, 
   c.ws_bytes = (size_t)SBP_NOALLOC_SCRATCH_BYTES; c.dev_status = dev_status;
   c.stream = static_cast<cudaStream_t>(stream);
   return run(c);
+}
+
+size_t sbp_mlp_workspace_bytes(int64_t T, int64_t d, int64_t f, int64_t chunk) {
+  MlpLayout L;
+  if (!mlp_layout(T, d, f, chunk, &L)) return 0;
+  return L.total;
+}
+
+int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, const void* dY, int64_t T, int64_t d,
+                            int64_t f, int64_t chunk, void* dX, float* dWgu, float* dWd, int accumulate,
+                            void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return run_mlp(X, Wgu, Wd, dY, T, d, f, chunk, dX, dWgu, dWd, accumulate, workspace, ws_bytes, dev_status,
+                 static_cast<cudaStream_t>(stream));
 }
 
 const char* sbp_status_string(int status) {

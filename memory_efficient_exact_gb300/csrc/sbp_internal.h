@@ -57,8 +57,22 @@ struct TcBwdArgs {
   float* dW; int dw_accumulate;
   uint32_t* counter;            // zero before launch
   int32_t* status;
+  int dw_only = 0;              // 1: only the dW units (no dH)
 };
 cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s);
+
+// SwiGLU-MLP pair GEMMs, sbp_mlp.cu.  da = false: g | u = x_c [Wg; Wu]^T with the
+// activation epilogue (B = packed Wgu [2f, d]); da = true: da = dY_c Wd with the
+// activation-backward epilogue (B = Wd [d, f]), in place over g | u.
+struct TcMlpArgs {
+  const void* Arows; int64_t T, d, f;  // x or dY [T, d] bf16
+  const void* B;                       // Wgu [2f, d] or Wd [d, f], bf16
+  int64_t r0; int rows;
+  void* Aout;                          // a = silu(g) u [rows, f] bf16 (da = false)
+  void* GU;                            // [rows, 2f] bf16
+  int32_t* status;
+};
+cudaError_t tc_mlp(const TcMlpArgs& a, bool da, cudaStream_t s);
 
 // SIMT fp32 kernels (fp32 operands), sbp_simt.cu
 cudaError_t simt_forward(const float* H, const float* W, int64_t d, int64_t V, int64_t r0, int rows,

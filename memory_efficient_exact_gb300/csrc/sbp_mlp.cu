@@ -1,0 +1,251 @@
+// Tensor-core kernels of the chunked SwiGLU-MLP backward (bf16, sm_103a).
+//
+// The position-wise MLP sublayer y = a Wd^T, a = silu(x Wg^T) * (x Wu^T), splits over row
+// chunks exactly as the LM head does: each chunk recomputes its activations and adds its
+// share of the weight gradients.  Two pair GEMMs are specific to it (the rest reuses
+// k_bwd):
+//   k_mlp<false>  gu = x_c [Wg; Wu]^T for one 128-wide block of f at a time: CTA 0 of the
+//                 pair stages gate rows, CTA 1 the matching up rows of the packed Wgu
+//                 [2f, d], so one 256-column accumulator tile holds g | u of the same f;
+//                 epilogue: a = silu(g) u (bf16), and g, u kept (bf16) for the backward.
+//   k_mlp<true>   da = dY_c Wd (B = Wd [d, f], MN-major); epilogue: dg = da u silu'(g),
+//                 du = da silu(g), written in place over g | u.
+// Same pair protocol, warp roles and bounded waits as the LM-head kernels.
+#include "sbp_tc_common.cuh"
+
+namespace sbp {
+namespace tc {
+
+struct MlpP {
+  int64_t r0; int rows; int64_t f;
+  int mt, ntn, kb;
+  __nv_bfloat16* A;    // [rows, f]   a = silu(g) u                (k_mlp<false>)
+  __nv_bfloat16* GU;   // [rows, 2f]  g | u, then dg | du in place
+  int32_t* status; uint64_t limit_ns;
+};
+
+constexpr size_t SMEM_MLP = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+constexpr uint32_t IDESC_KK = idesc_bf16(256, 256, false, false);
+constexpr uint32_t IDESC_KM = idesc_bf16(256, 256, false, true);
+
+__device__ __forceinline__ float sigmoid_fast(float t) { return __fdividef(1.f, 1.f + ex2(-t * L2E)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+
+template <bool DA>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    k_mlp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const MlpP p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ctarank();
+  prologue(c, warp);
+  const uint32_t tmem = c->tmem_base;
+  const int total = p.mt * p.ntn;
+  const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_map(&tmA);
+      prefetch_map(&tmB);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_phase[STAGES] = {0, 0, 0, 0, 0, 0};
+      bool ok = true;
+      for (int tile = pid; tile < total && ok; tile += npairs) {
+        const int mp = tile % p.mt, nb = tile / p.mt;
+        const int arow = (int)(p.r0 + (int64_t)mp * 256 + rank * 128);
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!wait_bounded(&c->empty[stage], phase ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
+          const uint32_t fb = mapa(saddr(&c->full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&c->full[stage], PAIR_TX);
+          tma_load_2d_pair(sa, &tmA, fb, kb * BK, arow);
+          if (!DA) {
+            // gate rows [128 nb, +128) in CTA 0, up rows [f + 128 nb, +128) in CTA 1
+            tma_load_2d_pair(sb, &tmB, fb, kb * BK, (int)((rank ? p.f : 0) + (int64_t)nb * 128));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(sb + j * BOX_BYTES, &tmB, fb, nb * BN + (int)rank * 128 + j * 64, kb * BK);
+          }
+          issued |= 1u << stage;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        fail(c, p.status);
+        if (rank == 0) drain_copies(c, last_phase, issued);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pid; tile < total && ok; tile += npairs, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!wait_cluster(&c->tempty[buf], (use & 1u) ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (!wait_bounded(&c->full[stage], phase, &c->abort, p.limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = saddr(base + stage * STAGE_BYTES), sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t bdesc =
+                DA ? sw128_desc(sb + k * 2048, BOX_BYTES, 1024) : sw128_desc(sb + k * 32, 16, 1024);
+            mma2_bf16(dt, sw128_desc(sa + k * 32, 16, 1024), bdesc, DA ? IDESC_KM : IDESC_KK, (kb | k) != 0);
+          }
+          commit2_mc(&c->empty[stage], 3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        commit2_mc(&c->tfull[buf], 3);
+      }
+      if (!ok) fail(c, p.status);
+      commit2_mc(&c->mdone, 1);
+      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int lrow = q * 32 + lane;
+    int local = 0;
+    for (int tile = pid; tile < total; tile += npairs, ++local) {
+      const int mp = tile % p.mt, nb = tile / p.mt;
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      const int row = mp * 256 + (int)rank * 128 + lrow;
+      const bool vrow = row < p.rows;
+      if (!warp_wait_cluster(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
+        fail(c, p.status);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      uint32_t r[4][32];
+      __syncwarp();
+      if (!DA) {
+        // g in accumulator columns [64h, 64h+64), u in [128 + 64h, 128 + 64h + 64)
+        tmem_ld32(tb + 64 * h, r[0]);
+        tmem_ld32(tb + 64 * h + 32, r[1]);
+        tmem_ld32(tb + 128 + 64 * h, r[2]);
+        tmem_ld32(tb + 128 + 64 * h + 32, r[3]);
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_ld32(tb + 128 * h + g * 32, r[g]);
+      }
+      tmem_ld_wait();
+      release_tmem(c, buf, lane);
+      if (!vrow) continue;
+      __nv_bfloat16* gu = p.GU + (int64_t)row * 2 * p.f;
+      if (!DA) {
+        const int64_t f0 = (int64_t)nb * 128 + 64 * h;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t av[16], gv[16], uv[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float g0 = __uint_as_float(r[g][j]), g1 = __uint_as_float(r[g][j + 1]);
+            const float u0 = __uint_as_float(r[2 + g][j]), u1 = __uint_as_float(r[2 + g][j + 1]);
+            av[j / 2] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
+            gv[j / 2] = pack_bf16(g0, g1);
+            uv[j / 2] = pack_bf16(u0, u1);
+          }
+          uint4* da = reinterpret_cast<uint4*>(p.A + (int64_t)row * p.f + f0 + 32 * g);
+          uint4* dg = reinterpret_cast<uint4*>(gu + f0 + 32 * g);
+          uint4* du = reinterpret_cast<uint4*>(gu + p.f + f0 + 32 * g);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            da[k] = make_uint4(av[4 * k], av[4 * k + 1], av[4 * k + 2], av[4 * k + 3]);
+            dg[k] = make_uint4(gv[4 * k], gv[4 * k + 1], gv[4 * k + 2], gv[4 * k + 3]);
+            du[k] = make_uint4(uv[4 * k], uv[4 * k + 1], uv[4 * k + 2], uv[4 * k + 3]);
+          }
+        }
+      } else {
+        const int64_t f0 = (int64_t)nb * BN + 128 * h;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4* pg = reinterpret_cast<uint4*>(gu + f0 + 32 * g);
+          uint4* pu = reinterpret_cast<uint4*>(gu + p.f + f0 + 32 * g);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 G4 = pg[k], U4 = pu[k];
+            const uint32_t gw[4] = {G4.x, G4.y, G4.z, G4.w}, uw[4] = {U4.x, U4.y, U4.z, U4.w};
+            uint32_t ow_g[4], ow_u[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 gg = unpack_bf16(gw[e]), uu = unpack_bf16(uw[e]);
+              const float a0 = __uint_as_float(r[g][8 * k + 2 * e]), a1 = __uint_as_float(r[g][8 * k + 2 * e + 1]);
+              const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
+              // dg = da u silu'(g), silu'(g) = s (1 + g (1 - s));  du = da silu(g)
+              ow_g[e] = pack_bf16(a0 * uu.x * s0 * (1.f + gg.x * (1.f - s0)),
+                                  a1 * uu.y * s1 * (1.f + gg.y * (1.f - s1)));
+              ow_u[e] = pack_bf16(a0 * gg.x * s0, a1 * gg.y * s1);
+            }
+            pg[k] = make_uint4(ow_g[0], ow_g[1], ow_g[2], ow_g[3]);
+            pu[k] = make_uint4(ow_u[0], ow_u[1], ow_u[2], ow_u[3]);
+          }
+        }
+      }
+    }
+  }
+  teardown(c, warp);
+}
+
+}  // namespace tc
+
+cudaError_t tc_mlp(const TcMlpArgs& a, bool da, cudaStream_t s) {
+  using namespace tc;
+  static int attr_done = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (attr_done == 0) {
+      const bool ok =
+          cudaFuncSetAttribute(k_mlp<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MLP) ==
+              cudaSuccess &&
+          cudaFuncSetAttribute(k_mlp<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MLP) ==
+              cudaSuccess;
+      attr_done = ok ? 1 : -1;
+    }
+    if (attr_done != 1) return cudaErrorInvalidConfiguration;
+  }
+  CUtensorMap mA, mB;
+  // A: x or dY rows [T, d], boxes of 64 (K) x 128 rows
+  if (!make_map(&mA, a.Arows, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;
+  if (!da) {
+    // B: the packed [Wg; Wu] = [2f, d], K-major boxes of 64 x 128 rows
+    if (!make_map(&mB, a.B, (uint64_t)a.d, (uint64_t)(2 * a.f), (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;
+  } else {
+    // B: Wd [d, f] read MN-major: boxes of 64 f-columns x 64 d-rows
+    if (!make_map(&mB, a.B, (uint64_t)a.f, (uint64_t)a.d, (uint64_t)a.f, 64, 64)) return cudaErrorInvalidValue;
+  }
+  MlpP p;
+  p.r0 = a.r0; p.rows = a.rows; p.f = a.f;
+  p.mt = (a.rows + 255) / 256;
+  p.ntn = da ? (int)(a.f / BN) : (int)(a.f / 128);
+  p.kb = (int)((a.d + BK - 1) / BK);
+  p.A = static_cast<__nv_bfloat16*>(a.Aout);
+  p.GU = static_cast<__nv_bfloat16*>(a.GU);
+  p.status = a.status; p.limit_ns = wait_limit_ns();
+  const int total = p.mt * p.ntn;
+  const void* kern = da ? (const void*)k_mlp<true> : (const void*)k_mlp<false>;
+  int pairs = max_pairs(kern, SMEM_MLP);
+  if (pairs > total) pairs = total;
+  if (da) k_mlp<true><<<2 * pairs, NUM_THREADS, SMEM_MLP, s>>>(mA, mB, p);
+  else k_mlp<false><<<2 * pairs, NUM_THREADS, SMEM_MLP, s>>>(mA, mB, p);
+  return cudaGetLastError();
+}
+
+}  // namespace sbp

@@ -55,6 +55,10 @@ def _load() -> ctypes.CDLL:
                                          SZ, P, P]
     lib.sbp_lmhead_sft_noalloc.restype = C
     lib.sbp_lmhead_sft_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, P]
+    lib.sbp_mlp_workspace_bytes.restype = SZ
+    lib.sbp_mlp_workspace_bytes.argtypes = [I64, I64, I64, I64]
+    lib.sbp_mlp_swiglu_backward.restype = C
+    lib.sbp_mlp_swiglu_backward.argtypes = [P, P, P, P, I64, I64, I64, I64, P, P, P, C, P, SZ, P, P]
     lib.sbp_status_string.restype = ctypes.c_char_p
     lib.sbp_status_string.argtypes = [C]
     lib.sbp_last_launch_count.restype = C
@@ -291,3 +295,36 @@ def check_status(status: torch.Tensor, where: str = "device") -> None:
     code = int(status.item())
     if code != OK:
         raise SbpError(code, where)
+
+
+def mlp_workspace_bytes(T: int, d: int, f: int, chunk: int) -> int:
+    return int(_lib.sbp_mlp_workspace_bytes(T, d, f, chunk))
+
+
+def mlp_swiglu_backward(X, Wgu, Wd, dY, chunk, *, dX=None, dWgu=None, dWd=None, accumulate=False, workspace=None,
+                        status=None, stream=None) -> dict:
+    """Chunked backward of the SwiGLU MLP sublayer (``sbp_mlp_swiglu_backward``).
+
+    X, dY [T, d] bf16; Wgu [2f, d] bf16 (gate rows then up rows); Wd [d, f] bf16."""
+    _dev(X, Wgu, Wd, dY)
+    T, d = X.shape
+    f = Wd.shape[1]
+    if Wgu.shape != (2 * f, d) or Wd.shape != (d, f) or dY.shape != (T, d):
+        raise ValueError("shapes: X, dY [T, d]; Wgu [2f, d]; Wd [d, f]")
+    if any(t.dtype != torch.bfloat16 for t in (X, Wgu, Wd, dY)):
+        raise TypeError("the MLP sublayer takes bf16 operands")
+    dev = X.device
+    if workspace is None:
+        n = mlp_workspace_bytes(T, d, f, chunk)
+        if n == 0:
+            raise SbpError(ERR_INVALID_ARG, "mlp_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    dX = torch.empty_like(X) if dX is None else dX
+    dWgu = torch.empty((2 * f, d), dtype=torch.float32, device=dev) if dWgu is None else dWgu
+    dWd = torch.empty((d, f), dtype=torch.float32, device=dev) if dWd is None else dWd
+    _dev(dX, dWgu, dWd)
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_mlp_swiglu_backward(_p(X), _p(Wgu), _p(Wd), _p(dY), T, d, f, chunk, _p(dX), _p(dWgu), _p(dWd),
+                                        int(bool(accumulate)), _p(workspace), workspace.numel(), _p(st),
+                                        _stream(stream)), "sbp_mlp_swiglu_backward")
+    return dict(dX=dX, dWgu=dWgu, dWd=dWd, status=st)
