@@ -405,6 +405,111 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------------ MLP sublayer
+
+MLP_WORKLOAD = dict(workload="swiglu_mlp_bwd_bf16_T16384_d4096_f12288_chunk4096", T=16384, d=4096, f=12288,
+                    chunk=4096, seed=1005)
+MLP_METRIC = "mlp sublayer bwd tokens/s (SwiGLU, d=4096, f=12288) and % BF16 tensor peak"
+
+
+def make_mlp_inputs(T, d, f, seed):
+    from memory_efficient_exact_gb300 import inputs as I
+    import numpy as np
+    g = np.random.default_rng(np.random.SeedSequence([seed, 11]))
+    X = I.round_bf16(g.standard_normal((T, d), dtype=np.float32))
+    Wgu = I.round_bf16(g.standard_normal((2 * f, d), dtype=np.float32) * np.float32(d ** -0.5))
+    Wd = I.round_bf16(g.standard_normal((d, f), dtype=np.float32) * np.float32(f ** -0.5))
+    dY = I.round_bf16(g.standard_normal((T, d), dtype=np.float32))
+    return X, Wgu, Wd, dY
+
+
+def run_mlp_bench(args):
+    import torch
+    from memory_efficient_exact_gb300 import _build
+    _build.build_library()
+    from memory_efficient_exact_gb300 import sbp
+    w = dict(MLP_WORKLOAD)
+    if args.chunk:
+        w["chunk"] = args.chunk
+    if args.tokens:
+        w["T"] = args.tokens
+    T, d, f, chunk = w["T"], w["d"], w["f"], w["chunk"]
+    w["workload"] = f"swiglu_mlp_bwd_bf16_T{T}_d{d}_f{f}_chunk{chunk}"
+    dev = torch.device("cuda", torch.cuda.current_device())
+    X, Wgu, Wd, dY = make_mlp_inputs(T, d, f, w["seed"])
+    bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16)
+    Xt, Wgut, Wdt, dYt = bf(X), bf(Wgu), bf(Wd), bf(dY)
+    ws = torch.empty(sbp.mlp_workspace_bytes(T, d, f, chunk), dtype=torch.uint8, device=dev)
+    dX = torch.empty_like(Xt)
+    dWgu = torch.empty((2 * f, d), dtype=torch.float32, device=dev)
+    dWd = torch.empty((d, f), dtype=torch.float32, device=dev)
+    st = torch.zeros((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return sbp.mlp_swiglu_backward(Xt, Wgut, Wdt, dYt, chunk, dX=dX, dWgu=dWgu, dWd=dWd, workspace=ws,
+                                       status=st, stream=stream)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sbp.check_status(st, "warm-up")
+    launches = sbp.last_launch_count()
+    clocks = ClockSampler(gpu_id_for(torch, dev))
+    time.sleep(0.3)
+    sbp.profile_read()
+    sbp.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sbp.profile_enable(False)
+    clk = clocks.stop()
+    prof = sbp.profile_read()
+    sbp.check_status(st, "timed region")
+    ms = e0.elapsed_time(e1)
+    value = T * args.steps / (ms / 1000.0)
+    peaks, src = load_peaks()
+    n_chunks = (T + chunk - 1) // chunk
+    up_ms, up_n = prof["forward_gemm"]      # recompute of g, u and the da GEMM (2 launches per chunk)
+    bw_ms, bw_n = prof["backward_gemm"]     # dX + [dWg; dWu] and dWd (2 launches per chunk)
+    executed = 16.0 * d * f                  # per token: recompute 4, da 2, dX 4, dWgu 4, dWd 2 (x d f)
+    bw_tf = 10.0 * d * f * T * args.steps / (bw_ms / 1000.0) / 1e12 if bw_n else None
+    fw_tf = 6.0 * d * f * T * args.steps / (up_ms / 1000.0) / 1e12 if up_n else None
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import mlp as OM
+        Ts = 128
+        t0 = time.perf_counter()
+        OM.backward(X[:Ts], Wgu[:f], Wgu[f:], Wd, dY[:Ts])
+        sec = time.perf_counter() - t0
+        cpu = {"value": Ts / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"first {Ts} tokens (full d={d}, f={f}), float64 numpy/BLAS, one run"}
+    line = {
+        "metric": MLP_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["workload"], "T": T, "d": d, "f": f, "chunk": chunk},
+        "roofline": {"kernel": "k_bwd on the MLP (dX + [dWg; dWu], dWd)", "bound": "tensor", "achieved": bw_tf,
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": bw_tf / peaks["bf16_tflops_sustained"] if bw_tf else None, "traffic": None,
+                     "peak_source": f"bf16 dense, sustained, {src}"},
+        "kernels": {"k_mlp (recompute + da)": {"achieved_tflops": fw_tf, "ms": up_ms, "launches": up_n},
+                    "k_bwd": {"achieved_tflops": bw_tf, "ms": bw_ms, "launches": bw_n},
+                    "other": {"ms": prof["other"][0], "launches": prof["other"][1]}},
+        "executed_tflops": executed * value / 1e12,
+        "pct_bf16_peak_executed": 100.0 * executed * value / 1e12 / peaks["bf16_tflops"],
+        "pct_bf16_peak_credited_12dF": 100.0 * 12.0 * d * f * value / 1e12 / peaks["bf16_tflops"],
+        "peak_source": src, "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+        "unchunked_activations_gb": 3 * T * f * 2 / 1e9,
+        "gpu_launches": launches * args.steps, "clocks": clk, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,6 +522,8 @@ def main(argv=None):
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
     ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
+    ap.add_argument("--sublayer", choices=["lmhead", "mlp"], default="lmhead",
+                    help="mlp: the chunked SwiGLU-MLP backward (its own JSON line)")
     ap.add_argument("--objective", choices=["sft", "grpo", "dpo"], default="sft",
                     help="grpo: 2048-token responses; dpo: 4096-token sequences, both passes per step")
     args = ap.parse_args(argv)
@@ -438,6 +545,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.sublayer == "mlp":
+        return run_mlp_bench(args)
     return run_ours(args)
 
 

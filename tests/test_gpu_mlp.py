@@ -64,5 +64,7 @@ def test_mlp_accumulate_and_determinism(sbp):
     acc_gu, acc_d = a["dWgu"].clone(), a["dWd"].clone()
     sbp.mlp_swiglu_backward(X, Wgu, Wd, dY, chunk, dWgu=acc_gu, dWd=acc_d, accumulate=True)
     torch.cuda.synchronize()
-    assert torch.allclose(acc_gu, 2 * a["dWgu"], rtol=1e-6, atol=1e-9)
-    assert torch.allclose(acc_d, 2 * a["dWd"], rtol=1e-6, atol=1e-9)
+    # the accumulated sum is ((a + c1) + c2) + c3 against 2 (c1 + c2 + c3): equal up to fp32
+    # rounding of the chunk terms, which cancel in part
+    for acc, ref in ((acc_gu, a["dWgu"]), (acc_d, a["dWd"])):
+        assert torch.allclose(acc, 2 * ref, rtol=1e-5, atol=1e-6 * ref.abs().max().item())
