@@ -89,7 +89,7 @@ int choose_splits(int64_t rows, int64_t d, int64_t V, int sms) {
   return s;
 }
 
-bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L) {
+bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L, int nbuf) {
   if (T < 0 || d < 1 || V < 1 || chunk < 1 || chunk > 65535) return false;
   if (dtype != SBP_BF16 && dtype != SBP_FP32) return false;
   if (mode < SBP_MODE_SFT || mode > SBP_MODE_DPO2) return false;
@@ -102,11 +102,18 @@ bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int 
   l.splits = dtype == SBP_BF16 ? choose_splits(l.chunk, d, V, num_sms()) : 1;
   l.n_chunks = T > 0 ? (T + l.chunk - 1) / l.chunk : 0;
   l.max_seq = T + 64;
+  if (nbuf == 0) nbuf = (dtype == SBP_BF16 && mode != SBP_MODE_DPO1 && l.n_chunks > 1) ? 2 : 1;
+  l.nbuf = nbuf;
   size_t o = 0;
   l.off_zg = o;      o = align256(o + (size_t)l.chunk * l.ldv * l.esize);
   l.off_part = o;    o = align256(o + (size_t)l.chunk * l.ntiles * sizeof(float2));
   l.off_zy = o;      o = align256(o + (size_t)l.chunk * sizeof(float));
   l.off_rowv = o;    o = align256(o + (size_t)l.chunk * sizeof(float));
+  if (nbuf == 2) {
+    l.off_zg2 = o;   o = align256(o + (size_t)l.chunk * l.ldv * l.esize);
+    l.off_part2 = o; o = align256(o + (size_t)l.chunk * l.ntiles * sizeof(float2));
+    l.off_rowv2 = o; o = align256(o + (size_t)l.chunk * sizeof(float));
+  }
   l.off_dhp = o;     o = align256(o + (size_t)l.splits * l.chunk * d * sizeof(float));
   l.off_tokloss = o; o = align256(o + (size_t)(T + 1) * sizeof(float));
   l.off_logp = o;    o = align256(o + (size_t)(T + 1) * sizeof(float));
@@ -310,7 +317,9 @@ __global__ void __launch_bounds__(256) k_grad(void* buf, int64_t ld, int64_t V, 
         const float s = sc[v0 / kStatW].x;
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] *= s;
-        if (y >= v0 && y < v0 + 8) f[y - v0] -= w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (v0 + i == (int64_t)y) f[i] -= w;
       }
       store8(g + v0, f);
     } else {
@@ -450,6 +459,7 @@ struct Call {
   const int32_t* cu; int n_seq; double* seq_logp; const double* seq_in; const double* ref_in;
   float beta; double* margins;
   void* ws; size_t ws_bytes; int32_t* dev_status; cudaStream_t stream;
+  int nbuf = 0;   // chunk buffer sets (0: default of make_layout)
 };
 
 #define SBP_CUDA(x)                        \
@@ -461,7 +471,7 @@ struct Call {
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int validate(const Call& c, Layout* L) {
-  if (!make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, L)) return SBP_ERR_INVALID_ARG;
+  if (!make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, L, c.nbuf)) return SBP_ERR_INVALID_ARG;
   if (c.T > 0 && (!c.H || !c.labels)) return SBP_ERR_INVALID_ARG;
   if (!c.W || !c.dev_status) return SBP_ERR_INVALID_ARG;
   if (c.T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
@@ -534,35 +544,52 @@ int run(const Call& c) {
   }
 
   const bool bf16 = c.dtype == SBP_BF16;
-  const size_t es = bf16 ? 2 : 4;
-  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
-    const int64_t r0 = ci * L.chunk;
-    const int rows = (int)((r0 + L.chunk <= c.T) ? L.chunk : c.T - r0);
-    const int32_t* yl = c.labels + r0;
-    // forward GEMM + row statistics
+  // buffer set b: the chunk's e / G values, tile partials (then scales), row weights
+  void* zgb[2] = {zg, L.nbuf == 2 ? ws + L.off_zg2 : zg};
+  float2* partb[2] = {part, L.nbuf == 2 ? reinterpret_cast<float2*>(ws + L.off_part2) : part};
+  float* wb[2] = {w_row, L.nbuf == 2 ? reinterpret_cast<float*>(ws + L.off_rowv2) : w_row};
+  auto r0_of = [&](int64_t ci) { return ci * L.chunk; };
+  auto rows_of = [&](int64_t ci) {
+    const int64_t r0 = r0_of(ci);
+    return (int)((r0 + L.chunk <= c.T) ? L.chunk : c.T - r0);
+  };
+
+  // forward GEMM + row statistics of chunk ci into buffer set b; on the tensor-core path it
+  // also forms chunk `prev`'s gradient (buffer set pb) between its tiles when prev >= 0
+  auto forward = [&](int64_t ci, int b, int64_t prev, int pb) -> int {
+    const int64_t r0 = r0_of(ci);
+    const int rows = rows_of(ci);
     if (bf16) {
       TcFwdArgs a{};
       a.H = c.H; a.W = c.W; a.T = c.T; a.d = c.d; a.V = c.V; a.r0 = r0; a.rows = rows;
-      a.labels = yl; a.ignore_index = c.ign;
-      a.E = grad ? zg : nullptr; a.lde = L.ldv; a.part = part; a.zy = zy; a.status = c.dev_status;
+      a.labels = c.labels + r0; a.ignore_index = c.ign;
+      a.E = grad ? zgb[b] : nullptr; a.lde = L.ldv; a.part = partb[b]; a.zy = zy; a.status = c.dev_status;
+      if (prev >= 0) {
+        a.gprev = zgb[pb]; a.part_prev = partb[pb]; a.w_prev = wb[pb];
+        a.y_prev = c.labels + r0_of(prev); a.rows_prev = rows_of(prev);
+      }
       prof::Scope ps(0, s);
       SBP_CUDA(tc_forward(a, s));
       ++launches;
     } else {
       prof::Scope ps(0, s);
       SBP_CUDA(simt_forward(static_cast<const float*>(c.H), static_cast<const float*>(c.W), c.d, c.V, r0, rows,
-                            yl, c.ign, static_cast<float*>(zg), L.ldv, part, zy, grad, s));
+                            c.labels + r0, c.ign, static_cast<float*>(zgb[b]), L.ldv, partb[b], zy, grad, s));
       launches += 2;
     }
-    // combine: lse, logp, weights, loss terms
+    return SBP_OK;
+  };
+  // lse, logp, weights, loss terms; the tile maxima become gradient scales
+  auto combine = [&](int64_t ci, int b) -> int {
+    const int64_t r0 = r0_of(ci);
+    const int rows = rows_of(ci);
     CombineArgs ca{};
-    ca.part = part; ca.ntiles = L.ntiles; ca.zy = zy; ca.labels = yl; ca.rows = rows; ca.r0 = r0;
-    ca.V = c.V; ca.ign = c.ign; ca.nvalid = nvalid; ca.w_row = w_row; ca.logp = logp; ca.tokloss = tokloss;
+    ca.part = partb[b]; ca.ntiles = L.ntiles; ca.zy = zy; ca.labels = c.labels + r0; ca.rows = rows; ca.r0 = r0;
+    ca.V = c.V; ca.ign = c.ign; ca.nvalid = nvalid; ca.w_row = wb[b]; ca.logp = logp; ca.tokloss = tokloss;
     ca.adv = c.adv; ca.logp_old = c.logp_old; ca.clip_lo = c.clip_lo; ca.clip_hi = c.clip_hi;
     ca.cu = c.cu; ca.n_seq = c.n_seq; ca.seqw = seqw;
     ca.ref_logp = c.ref_logp; ca.kl_coef = c.kl_coef;
     const unsigned gc = (unsigned)((rows + 7) / 8);
-    {
     prof::Scope ps(3, s);
     switch (c.mode) {
       case SBP_MODE_SFT: k_combine<SBP_MODE_SFT><<<gc, 256, 0, s>>>(ca); break;
@@ -570,37 +597,43 @@ int run(const Call& c) {
       case SBP_MODE_DPO1: k_combine<SBP_MODE_DPO1><<<gc, 256, 0, s>>>(ca); break;
       default: k_combine<SBP_MODE_DPO2><<<gc, 256, 0, s>>>(ca); break;
     }
-    }
     ++launches;
     SBP_CUDA(cudaGetLastError());
-    if (!grad) continue;
-    // logit gradient, in place
-    {
-      const int64_t vec = (c.V + 7) / 8;
-      dim3 g((unsigned)((vec + 255) / 256), (unsigned)rows);
-      prof::Scope ps(2, s);
-      if (bf16) k_grad<__half, __nv_bfloat16><<<g, 256, 0, s>>>(zg, L.ldv, c.V, part, L.ntiles, w_row, yl);
-      else k_grad<float, float><<<g, 256, 0, s>>>(zg, L.ldv, c.V, part, L.ntiles, w_row, yl);
-      ++launches;
-      SBP_CUDA(cudaGetLastError());
-    }
-    // dH_c = G_c W and dW (+)= G_c^T H_c
+    return SBP_OK;
+  };
+  // standalone logit gradient, in place
+  auto gradient = [&](int64_t ci, int b) -> int {
+    const int64_t vec = (c.V + 7) / 8;
+    dim3 g((unsigned)((vec + 255) / 256), (unsigned)rows_of(ci));
+    prof::Scope ps(2, s);
+    if (bf16)
+      k_grad<__half, __nv_bfloat16><<<g, 256, 0, s>>>(zgb[b], L.ldv, c.V, partb[b], L.ntiles, wb[b],
+                                                       c.labels + r0_of(ci));
+    else
+      k_grad<float, float><<<g, 256, 0, s>>>(zgb[b], L.ldv, c.V, partb[b], L.ntiles, wb[b], c.labels + r0_of(ci));
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+    return SBP_OK;
+  };
+  // dH_c = G_c W and dW (+)= G_c^T H_c, then dH_c's split partials -> dH rows
+  auto backward = [&](int64_t ci, int b) -> int {
+    const int64_t r0 = r0_of(ci);
+    const int rows = rows_of(ci);
     const int dw_acc = (ci > 0 || c.accumulate_dW) ? 1 : 0;
     int splits = 1;
     if (bf16) {
-      TcBwdArgs b{};
-      b.G = zg; b.ldg = L.ldv; b.H = c.H; b.W = c.W; b.T = c.T; b.d = c.d; b.V = c.V;
-      b.r0 = r0; b.rows = rows;
-      splits = choose_splits(rows, c.d, c.V, num_sms());
-      if (splits > L.splits) splits = L.splits;
-      b.splits = splits; b.dh_part = dhp; b.dW = c.dW; b.dw_accumulate = dw_acc;
-      b.counter = counters + ci; b.status = c.dev_status;
+      TcBwdArgs bw{};
+      bw.G = zgb[b]; bw.ldg = L.ldv; bw.H = c.H; bw.W = c.W; bw.T = c.T; bw.d = c.d; bw.V = c.V;
+      bw.r0 = r0; bw.rows = rows;
+      splits = std::min(choose_splits(rows, c.d, c.V, num_sms()), L.splits);
+      bw.splits = splits; bw.dh_part = dhp; bw.dW = c.dW; bw.dw_accumulate = dw_acc;
+      bw.counter = counters + ci; bw.status = c.dev_status;
       prof::Scope ps(1, s);
-      SBP_CUDA(tc_backward(b, s));
+      SBP_CUDA(tc_backward(bw, s));
       ++launches;
     } else {
       prof::Scope ps(1, s);
-      SBP_CUDA(simt_backward(static_cast<const float*>(zg), L.ldv, static_cast<const float*>(c.H),
+      SBP_CUDA(simt_backward(static_cast<const float*>(zgb[b]), L.ldv, static_cast<const float*>(c.H),
                              static_cast<const float*>(c.W), c.d, c.V, r0, rows, dhp, c.dW, dw_acc, s));
       launches += 2;
     }
@@ -608,13 +641,51 @@ int run(const Call& c) {
     prof::Scope ps(3, s);
     if (bf16)
       k_dh_reduce<__nv_bfloat16><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
-          dhp, splits, n, (int64_t)rows * c.d, static_cast<__nv_bfloat16*>(c.dH) + r0 * c.d);
+          dhp, splits, n, n, static_cast<__nv_bfloat16*>(c.dH) + r0 * c.d);
     else
       k_dh_reduce<float><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
-          dhp, splits, n, (int64_t)rows * c.d, static_cast<float*>(c.dH) + r0 * c.d);
+          dhp, splits, n, n, static_cast<float*>(c.dH) + r0 * c.d);
     ++launches;
     SBP_CUDA(cudaGetLastError());
+    return SBP_OK;
+  };
+
+#define SBP_TRY(x)                      \
+  do {                                  \
+    const int st_ = (x);                \
+    if (st_ != SBP_OK) return st_;      \
+  } while (0)
+
+  if (!grad) {
+    for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+      SBP_TRY(forward(ci, 0, -1, 0));
+      SBP_TRY(combine(ci, 0));
+    }
+  } else if (L.nbuf == 2 && bf16) {
+    // chunk ci's gradient forms inside chunk ci+1's forward (two buffer sets):
+    //   F0 C0 | F1(+G0) C1 B0 | F2(+G1) C2 B1 | ... | G_last B_last
+    SBP_TRY(forward(0, 0, -1, 0));
+    SBP_TRY(combine(0, 0));
+    for (int64_t ci = 1; ci < L.n_chunks; ++ci) {
+      const int b = (int)(ci & 1), pb = b ^ 1;
+      SBP_TRY(forward(ci, b, ci - 1, pb));
+      SBP_TRY(combine(ci, b));
+      SBP_TRY(backward(ci - 1, pb));
+    }
+    const int64_t last = L.n_chunks - 1;
+    if (last >= 0) {
+      SBP_TRY(gradient(last, (int)(last & 1)));
+      SBP_TRY(backward(last, (int)(last & 1)));
+    }
+  } else {
+    for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+      SBP_TRY(forward(ci, 0, -1, 0));
+      SBP_TRY(combine(ci, 0));
+      SBP_TRY(gradient(ci, 0));
+      SBP_TRY(backward(ci, 0));
+    }
   }
+#undef SBP_TRY
 
   if (c.mode == SBP_MODE_SFT || c.mode == SBP_MODE_GRPO) {
     k_loss_final<<<1, 1024, 0, s>>>(tokloss, c.T, nvalid, c.loss, c.n_valid);
@@ -633,7 +704,6 @@ int run(const Call& c) {
   if (c.logp_out && c.T > 0)
     SBP_CUDA(cudaMemcpyAsync(c.logp_out, logp, (size_t)c.T * sizeof(float), cudaMemcpyDeviceToDevice, s));
   g_launches = launches;
-  (void)es;
   return SBP_OK;
 }
 
@@ -850,7 +920,7 @@ int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels, 
                            void* stream) {
   if (!loss) return SBP_ERR_INVALID_ARG;
   Layout L;
-  if (!make_layout(T, d, V, chunk, dtype, SBP_MODE_SFT, &L)) return SBP_ERR_INVALID_ARG;
+  if (!make_layout(T, d, V, chunk, dtype, SBP_MODE_SFT, &L, 1)) return SBP_ERR_INVALID_ARG;
   if (L.total > (size_t)SBP_NOALLOC_SCRATCH_BYTES) return SBP_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
@@ -861,6 +931,7 @@ int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels, 
   c.dH = dH; c.dW = dW; c.accumulate_dW = accumulate_dW; c.ws = scratch;
   c.ws_bytes = (size_t)SBP_NOALLOC_SCRATCH_BYTES; c.dev_status = dev_status;
   c.stream = static_cast<cudaStream_t>(stream);
+  c.nbuf = 1;   // one buffer set: the gradient of each chunk runs as its own pass
   return run(c);
 }
 

@@ -18,17 +18,20 @@ struct Layout {
   int64_t T = 0, d = 0, V = 0, chunk = 0;  // chunk = rows of the largest chunk (<= T)
   int dtype = 0, mode = 0;
   int64_t ldv = 0;      // row stride (elements) of the chunk logit/gradient buffer
+  int nbuf = 1;         // chunk buffers: 2 lets chunk c's gradient form inside chunk c+1's forward
   int64_t ntiles = 0;   // row-statistics tiles per row = ceil(V / kStatW)
   int splits = 1;       // dH split-K factor (tensor-core path)
   size_t esize = 0;     // bytes per element of the chunk buffer
   size_t off_zg = 0, off_part = 0, off_zy = 0, off_rowv = 0, off_dhp = 0;
+  size_t off_zg2 = 0, off_part2 = 0, off_rowv2 = 0;   // second buffer set (nbuf = 2)
   size_t off_tokloss = 0, off_logp = 0, off_seqw = 0, off_scal = 0, off_cnt = 0;
   int64_t n_chunks = 0, max_seq = 0;
   size_t total = 0;
 };
 
 // Fills `L`; returns false for arguments no call can accept.
-bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L);
+bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L,
+                 int nbuf = 0);   // 0: the entry points' default (2 for bf16 gradients, else 1)
 
 // dH split-K factor of the tensor-core backward kernel for a chunk of `rows` rows.
 int choose_splits(int64_t rows, int64_t d, int64_t V, int num_sms);
@@ -45,6 +48,10 @@ struct TcFwdArgs {
   void* E; int64_t lde;    // fp16 exp(z - tile max), [rows, lde]; nullptr: statistics only
   float2* part; float* zy;
   int32_t* status;
+  // optional: the previous chunk's logit gradient, formed in place by this launch's
+  // epilogue warps between tiles (G = e * scale - w [v = y], fp16 -> bf16)
+  void* gprev = nullptr; const float2* part_prev = nullptr; const float* w_prev = nullptr;
+  const int32_t* y_prev = nullptr; int rows_prev = 0;
 };
 cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s);
 

@@ -40,7 +40,64 @@ struct FwdP {
   __half* E; int64_t lde;
   float2* part; int64_t ntiles; float* zy;
   int32_t* status; uint64_t limit_ns;
+  int stall;   // failure-detection test: the MMA thread first waits on a barrier nothing arrives on
+  // The previous chunk's logit gradient, formed by the epilogue warps in the time they
+  // do not need for this chunk's tiles: G = e * scale - w [v = y], fp16 -> bf16 in place.
+  __half* gprev;              // nullptr: no previous chunk to convert
+  const float2* part_prev;    // its tile scales
+  const float* w_prev;        // its row weights
+  const int32_t* y_prev;      // its labels
+  int rows_prev;
 };
+
+// A slice of the previous chunk's gradient conversion: this CTA owns a contiguous range of
+// its rows; epilogue thread t takes the 8-column vectors t, t + 256, ... of that range
+// (consecutive threads touch consecutive 16-byte vectors).
+struct SideJob {
+  int64_t rbeg, nvec, next, end;   // vector cursor of this thread, flat index over [rbeg, rend) x nvec
+};
+
+__device__ __forceinline__ void side_vector(const FwdP& p, int64_t r, int64_t v0) {
+  __half* e = p.gprev + r * p.lde;
+  __nv_bfloat16* g = reinterpret_cast<__nv_bfloat16*>(e);
+  const float w = p.w_prev[r];
+  const int32_t y = p.y_prev[r];
+  if (v0 + 8 <= p.V) {
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (w != 0.f) {
+      const uint4 in = *reinterpret_cast<const uint4*>(e + v0);
+      const float s = p.part_prev[r * p.ntiles + v0 / kStatW].x;
+      const __half2* hin = reinterpret_cast<const __half2*>(&in);
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __half22float2(hin[i]);
+        f[2 * i] = x.x * s;
+        f[2 * i + 1] = x.y * s;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (v0 + i == (int64_t)y) f[i] -= w;
+      __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    }
+    *reinterpret_cast<uint4*>(g + v0) = out;
+  } else {
+    for (int64_t v = v0; v < p.V; ++v) {
+      const float x = w == 0.f ? 0.f : __half2float(e[v]) * p.part_prev[r * p.ntiles + v / kStatW].x -
+                                          (v == y ? w : 0.f);
+      g[v] = __float2bfloat16_rn(x);
+    }
+  }
+}
+
+__device__ __forceinline__ void side_run(const FwdP& p, SideJob& j, int64_t quota) {
+  for (int64_t k = 0; k < quota && j.next < j.end; ++k, j.next += NUM_EPI_WARPS * 32) {
+    const int64_t r = j.rbeg + j.next / j.nvec;
+    side_vector(p, r, (j.next % j.nvec) * 8);
+  }
+}
 
 // =================================================================================== backward
 
@@ -107,7 +164,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0 && rank == 0) {
       int stage = 0, local = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      // injected stall: mdone completes only after the commit below, so this wait runs
+      // out, and every role of the pair takes the bounded-abort path
+      bool ok = !p.stall || wait_bounded(&c->mdone, 0, &c->abort, p.limit_ns);
       for (int tile = pid; tile < total && ok; tile += npairs, ++local) {
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
@@ -136,6 +195,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int lrow = q * 32 + lane;
+    // this thread's share of the previous chunk's gradient conversion, spread evenly over
+    // the tiles this CTA's epilogue handles
+    SideJob sj{0, 1, 0, 0};
+    int64_t quota = 0;
+    if (p.gprev) {
+      const int64_t rbeg = (int64_t)blockIdx.x * p.rows_prev / gridDim.x;
+      const int64_t rend = (int64_t)(blockIdx.x + 1) * p.rows_prev / gridDim.x;
+      sj.rbeg = rbeg;
+      sj.nvec = (p.V + 7) / 8;
+      sj.next = (warp - 2) * 32 + lane;
+      sj.end = (rend - rbeg) * sj.nvec;
+      const int64_t mine = sj.end > sj.next ? (sj.end - sj.next + NUM_EPI_WARPS * 32 - 1) / (NUM_EPI_WARPS * 32) : 0;
+      const int64_t ntiles_here = pid < total ? (total - pid + npairs - 1) / npairs : 0;
+      quota = ntiles_here > 0 ? (mine + ntiles_here - 1) / ntiles_here : mine;
+    }
     int local = 0;
     for (int tile = pid; tile < total; tile += npairs, ++local) {
       const int mp = tile % mtp, nb = tile / mtp;
@@ -218,7 +292,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int64_t tix = (int64_t)nb * 2 + h;
       if (vrow && tix < p.ntiles) p.part[(int64_t)row * p.ntiles + tix] = make_float2(m, s);
       if (vrow && has_y) p.zy[row] = zyv;
+      if (p.gprev) side_run(p, sj, quota);
     }
+    if (p.gprev && !c->abort) side_run(p, sj, INT64_MAX);   // what rounding left over
   }
   teardown(c, warp);
 }
@@ -497,6 +573,9 @@ cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
   p.E = static_cast<__half*>(a.E); p.lde = a.lde;
   p.part = a.part; p.ntiles = (a.V + kStatW - 1) / kStatW; p.zy = a.zy;
   p.status = a.status; p.limit_ns = wait_limit_ns();
+  p.stall = fault_stall_requested();
+  p.gprev = static_cast<__half*>(a.gprev); p.part_prev = a.part_prev; p.w_prev = a.w_prev;
+  p.y_prev = a.y_prev; p.rows_prev = a.rows_prev;
   const int total = p.mt * p.ntn;
   int pairs = max_pairs((const void*)k_fwd, SMEM_FWD);
   if (pairs > total) pairs = total;

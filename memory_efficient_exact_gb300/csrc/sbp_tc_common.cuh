@@ -344,6 +344,15 @@ inline bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Failure-detection test hook: SBP_FAULT_STALL=1 makes the next forward kernels stall
+// on purpose (read at every launch, so a test can switch it off again).  Together with a
+// short SBP_WAIT_LIMIT_MS it exercises the bounded-wait abort path: status
+// SBP_ERR_TIMEOUT, copies drained, tensor memory freed, the context still usable.
+inline int fault_stall_requested() {
+  const char* e = std::getenv("SBP_FAULT_STALL");
+  return (e && e[0] == '1') ? 1 : 0;
+}
+
 inline uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* e = std::getenv("SBP_WAIT_LIMIT_MS");

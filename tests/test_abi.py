@@ -44,8 +44,14 @@ def test_workspace_bytes(sbp):
     V, d = 151936, 4096
     w1 = sbp.workspace_bytes(16384, d, V, 2048, sbp.BF16, sbp.MODE_SFT)
     w2 = sbp.workspace_bytes(65536, d, V, 2048, sbp.BF16, sbp.MODE_SFT)
-    assert w1 > 2048 * V * 2                       # at least one chunk of logits (fp16/bf16)
-    assert w1 < 2048 * V * 2 * 2                   # ... and far below two
+    # two chunk buffers of logits (fp16/bf16): chunk c's gradient forms while chunk c+1's
+    # forward runs; a single chunk needs only one
+    assert w1 > 2 * 2048 * V * 2
+    assert w1 < 3 * 2048 * V * 2
+    w_one = sbp.workspace_bytes(2048, d, V, 2048, sbp.BF16, sbp.MODE_SFT)
+    assert 2048 * V * 2 < w_one < 2 * 2048 * V * 2
+    # DPO pass 1 forms no gradient: one buffer
+    assert sbp.workspace_bytes(16384, d, V, 2048, sbp.BF16, sbp.MODE_DPO1) < 2 * 2048 * V * 2
     assert w2 - w1 < 64 * 65536                    # T enters only through O(T) scalars
     assert sbp.workspace_bytes(16384, d, V, 4096, sbp.BF16, sbp.MODE_SFT) > w1
     # fp32 path keeps fp32 logits
