@@ -198,6 +198,31 @@ def test_edge_cases(sbp, dtype):
     check_grads(dtype, o1, ref, y)
 
 
+@pytest.mark.parametrize("dtype,T,d,V,chunk,label", [
+    ("bf16", 1, 128, 1000, 1, None),          # a single token
+    ("bf16", 64, 16, 256, 16, None),          # d far below one 64-wide k-block
+    ("bf16", 700, 256, 2000, 320, None),      # last chunk of 60 rows
+    ("bf16", 100, 128, 1000, 64, "last"),     # every label on the last column (V-tail tile)
+    ("fp32", 100, 32, 333, 64, "last"),
+    ("bf16", 300, 128, 1000, 128, "zero"),    # every label on column 0
+])
+def test_edge_shapes_and_labels(sbp, dtype, T, d, V, chunk, label):
+    H, W, y = make_case(T, d, V, dtype, seed=23 + T + d, w_std=0.2)
+    if label == "last":
+        y[y != IGN] = V - 1
+    elif label == "zero":
+        y[y != IGN] = 0
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    out = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.sft(H, W, y, IGN)
+    tol = TOL[dtype]
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= tol["loss"]
+    check_grads(dtype, out, ref, y)
+
+
 def test_label_out_of_range_sets_device_status(sbp):
     H, W, y = make_case(40, 64, 256, "bf16", seed=8)
     y[5] = 256
