@@ -1,0 +1,79 @@
+"""CPU oracle for the chunked backward of causal multi-head self-attention (float64).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/lmhead.py``): only the tests, the smoke check
+and the benchmark's CPU leg use it.
+
+StreamBP decomposes the chain rule along the sequence layer by layer and uses the causal
+structure: a chunk of queries only needs the keys and values up to its own position
+(chatpaper.ai / fugumt.com abstract; atlas.scime.ai summary, "Approach").  So the
+attention backward can run one query chunk at a time: chunk c (rows [c0, c1)) touches
+keys [0, c1) only, writes its dQ rows, and adds its share to dK and dV of those keys.
+
+Reading (the pages give no layer formula): per head, with scale s,
+    S = s Q K^T (causal: S_ij = -inf for j > i),  P = softmax_rows(S) = exp(S - lse),
+    O = P V;   given dO:  D_i = sum_k dO_ik O_ik,  dP = dO V^T,  dS = P * (dP - D),
+    dQ = s dS K,  dK = s dS^T Q,  dV = P^T dO.
+The forward's per-row log-sum-exp (lse) and output O are inputs, as a
+FlashAttention-style forward saves them.  Tensors are [H, T, hd].
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def forward(Q, K, V, scale: float) -> dict:
+    """O and lse per head, causal, unchunked."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    H, T, _ = Q.shape
+    mask = np.triu(np.ones((T, T), dtype=bool), k=1)
+    O = np.empty_like(Q)
+    lse = np.empty((H, T))
+    for h in range(H):
+        S = scale * (Q[h] @ K[h].T)
+        S[mask] = -np.inf
+        m = S.max(axis=1)
+        lse[h] = m + np.log(np.exp(S - m[:, None]).sum(axis=1))
+        O[h] = np.exp(S - lse[h][:, None]) @ V[h]
+    return dict(O=O, lse=lse)
+
+
+def backward(Q, K, V, O, dO, lse, scale: float) -> dict:
+    """dQ, dK, dV, unchunked (all queries at once)."""
+    Q, K, V, O, dO, lse = (_f64(a) for a in (Q, K, V, O, dO, lse))
+    H, T, _ = Q.shape
+    mask = np.triu(np.ones((T, T), dtype=bool), k=1)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h in range(H):
+        S = scale * (Q[h] @ K[h].T)
+        P = np.exp(S - lse[h][:, None])
+        P[mask] = 0.0
+        D = (dO[h] * O[h]).sum(axis=1)
+        dP = dO[h] @ V[h].T
+        dS = P * (dP - D[:, None])
+        dQ[h] = scale * (dS @ K[h])
+        dK[h] = scale * (dS.T @ Q[h])
+        dV[h] = P.T @ dO[h]
+    return dict(dQ=dQ, dK=dK, dV=dV)
+
+
+def backward_chunked(Q, K, V, O, dO, lse, scale: float, chunk: int) -> dict:
+    """The same backward one query chunk at a time: chunk [c0, c1) uses keys [0, c1)."""
+    Q, K, V, O, dO, lse = (_f64(a) for a in (Q, K, V, O, dO, lse))
+    H, T, _ = Q.shape
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h in range(H):
+        for c0 in range(0, T, chunk):
+            c1 = min(T, c0 + chunk)
+            S = scale * (Q[h, c0:c1] @ K[h, :c1].T)
+            P = np.exp(S - lse[h, c0:c1][:, None])
+            P[np.arange(c0, c1)[:, None] < np.arange(c1)[None, :]] = 0.0
+            D = (dO[h, c0:c1] * O[h, c0:c1]).sum(axis=1)
+            dS = P * (dO[h, c0:c1] @ V[h, :c1].T - D[:, None])
+            dQ[h, c0:c1] = scale * (dS @ K[h, :c1])
+            dK[h, :c1] += scale * (dS.T @ Q[h, c0:c1])
+            dV[h, :c1] += P.T @ dO[h, c0:c1]
+    return dict(dQ=dQ, dK=dK, dV=dV)

@@ -1,0 +1,87 @@
+"""Pins of the causal-attention oracle (CPU only): finite differences of sum(O * dO)
+through the forward, PyTorch's scaled_dot_product_attention with autograd in float64
+(library routine), the forward against a plain softmax, and chunked == unchunked
+(the causal chunk decomposition is exact)."""
+import numpy as np
+import pytest
+
+from oracle import attention as A
+
+
+def tiny(H=2, T=7, hd=4, seed=0):
+    g = np.random.default_rng(seed)
+    return (g.standard_normal((H, T, hd)), g.standard_normal((H, T, hd)), g.standard_normal((H, T, hd)),
+            g.standard_normal((H, T, hd)))
+
+
+def test_forward_matches_plain_softmax():
+    sp = pytest.importorskip("scipy.special")
+    Q, K, V, _ = tiny(seed=1)
+    f = A.forward(Q, K, V, 0.5)
+    for h in range(2):
+        S = 0.5 * Q[h] @ K[h].T
+        S[np.triu(np.ones((7, 7), bool), 1)] = -np.inf
+        np.testing.assert_allclose(f["O"][h], sp.softmax(S, axis=1) @ V[h], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(f["lse"][h], sp.logsumexp(S, axis=1), rtol=1e-14)
+
+
+def test_fd_of_sum_O_dO():
+    Q, K, V, dO = tiny(seed=2)
+    s = 0.7
+    f = A.forward(Q, K, V, s)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+
+    def loss():
+        return float((A.forward(Q, K, V, s)["O"] * dO).sum())
+
+    for X, key in ((Q, "dQ"), (K, "dK"), (V, "dV")):
+        G = np.zeros_like(X)
+        it = np.nditer(X, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            old = X[i]
+            X[i] = old + 1e-6
+            lp = loss()
+            X[i] = old - 1e-6
+            lm = loss()
+            X[i] = old
+            G[i] = (lp - lm) / 2e-6
+        np.testing.assert_allclose(b[key], G, rtol=1e-6, atol=1e-8)
+
+
+def test_matches_torch_sdpa_autograd_fp64():
+    torch = pytest.importorskip("torch")
+    Q, K, V, dO = tiny(H=3, T=9, hd=5, seed=3)
+    s = 0.4
+    f = A.forward(Q, K, V, s)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+    q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True, scale=s)[0]
+    o.backward(torch.tensor(dO))
+    np.testing.assert_allclose(f["O"], o.detach().numpy(), rtol=1e-12, atol=1e-13)
+    for t, key in ((q, "dQ"), (k, "dK"), (v, "dV")):
+        np.testing.assert_allclose(b[key], t.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 7])
+def test_chunked_equals_unchunked(chunk):
+    Q, K, V, dO = tiny(H=2, T=7, hd=3, seed=4)
+    f = A.forward(Q, K, V, 0.6)
+    a = A.backward(Q, K, V, f["O"], dO, f["lse"], 0.6)
+    b = A.backward_chunked(Q, K, V, f["O"], dO, f["lse"], 0.6, chunk)
+    for k in ("dQ", "dK", "dV"):
+        np.testing.assert_allclose(b[k], a[k], rtol=1e-12, atol=1e-13)
+
+
+def test_planted_missing_causal_mask_is_caught(monkeypatch):
+    Q, K, V, dO = tiny(seed=5)
+    f = A.forward(Q, K, V, 0.5)
+    real = np.triu
+
+    def no_mask(m, k=0):                 # the backward forgets the causal mask
+        return np.zeros_like(real(m, k))
+    monkeypatch.setattr(np, "triu", no_mask)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], 0.5)
+    monkeypatch.setattr(np, "triu", real)
+    ref = A.backward(Q, K, V, f["O"], dO, f["lse"], 0.5)
+    assert np.abs(b["dV"] - ref["dV"]).max() > 1e-3
