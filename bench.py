@@ -510,6 +510,108 @@ def run_mlp_bench(args):
     return 0
 
 
+# ------------------------------------------------------------------- causal attention
+
+ATTN_WORKLOAD = dict(H=32, T=8192, hd=128, chunk=1024, seed=1006)
+ATTN_METRIC = "attention bwd tokens/s (causal, H=32, hd=128, T=8192)"
+
+
+def attn_forward_inputs(torch, Q, K, V, scale):
+    """O and the row log-sum-exp of the causal forward, head by head in fp32 (input set-up
+    with plain torch ops, outside the timed region)."""
+    H, T, hd = Q.shape
+    O = torch.empty_like(Q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=Q.device)
+    mask = torch.ones((T, T), dtype=torch.bool, device=Q.device).triu(1)
+    for h in range(H):
+        S = (Q[h].float() @ K[h].float().T) * scale
+        S.masked_fill_(mask, float("-inf"))
+        l = torch.logsumexp(S, dim=1)
+        lse[h] = l
+        O[h] = (torch.exp(S - l[:, None]) @ V[h].float()).to(Q.dtype)
+    return O, lse
+
+
+def run_attn_bench(args):
+    import numpy as np
+    import torch
+    from memory_efficient_exact_gb300 import _build
+    _build.build_library()
+    from memory_efficient_exact_gb300 import sbp
+    w = dict(ATTN_WORKLOAD)
+    if args.chunk:
+        w["chunk"] = args.chunk
+    if args.tokens:
+        w["T"] = args.tokens
+    H, T, hd, chunk = w["H"], w["T"], w["hd"], w["chunk"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev).manual_seed(w["seed"])
+    Q, K, V, dO = (torch.randn((H, T, hd), device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    scale = hd ** -0.5
+    O, lse = attn_forward_inputs(torch, Q, K, V, scale)
+    ws = torch.empty(sbp.attn_workspace_bytes(H, T, hd, chunk), dtype=torch.uint8, device=dev)
+    dQ = torch.empty_like(Q)
+    dK = torch.empty((H, T, hd), dtype=torch.float32, device=dev)
+    dV = torch.empty((H, T, hd), dtype=torch.float32, device=dev)
+    st = torch.zeros((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return sbp.attn_causal_backward(Q, K, V, O, dO, lse, scale, chunk, dQ=dQ, dK=dK, dV=dV, workspace=ws,
+                                        status=st, stream=stream)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sbp.check_status(st, "warm-up")
+    launches = sbp.last_launch_count()
+    clocks = ClockSampler(gpu_id_for(torch, dev))
+    time.sleep(0.3)
+    sbp.profile_read()
+    sbp.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sbp.profile_enable(False)
+    clk = clocks.stop()
+    prof = sbp.profile_read()
+    sbp.check_status(st, "timed region")
+    ms = e0.elapsed_time(e1)
+    value = T * args.steps / (ms / 1000.0)
+    peaks, src = load_peaks()
+    # algorithmic FLOPs: per head and chunk, five GEMMs of 2 hd rows L (S, dP, dQ, dK, dV),
+    # L = the chunk's keys; the causal upper triangle of the diagonal block is included
+    rowkeys = sum(min(chunk, T - c0) * min(T, c0 + chunk) for c0 in range(0, T, chunk))
+    flops = 5 * 2 * hd * H * rowkeys
+    # chunk buffers: P and dS written once and read twice each (2 bytes an element)
+    pds_bytes = 12 * H * rowkeys
+    sp_ms, sp_n = prof["forward_gemm"]
+    bw_ms, bw_n = prof["backward_gemm"]
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"causal_attn_bwd_bf16_H{H}_T{T}_hd{hd}_chunk{chunk}", "H": H, "T": T, "hd": hd,
+                   "chunk": chunk},
+        "executed_tflops": flops * args.steps / (ms / 1000.0) / 1e12,
+        "pct_bf16_peak": 100.0 * flops * args.steps / (ms / 1000.0) / 1e12 / peaks["bf16_tflops"],
+        "chunk_buffer_gbs": pds_bytes * args.steps / (ms / 1000.0) / 1e9,
+        "kernels": {"k_attn (P, dS)": {"ms": sp_ms, "launches": sp_n,
+                                      "tflops": 4 * hd * H * rowkeys * args.steps / (sp_ms / 1000.0) / 1e12 if sp_n else None},
+                    "k_bwd (dQ + dK, dV)": {"ms": bw_ms, "launches": bw_n,
+                                            "tflops": 6 * hd * H * rowkeys * args.steps / (bw_ms / 1000.0) / 1e12 if bw_n else None},
+                    "other": {"ms": prof["other"][0], "launches": prof["other"][1]}},
+        "peak_source": src, "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+        "unchunked_scores_gb": H * T * T * 2 * 2 / 1e9,
+        "gpu_launches": launches * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,8 +624,8 @@ def main(argv=None):
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
     ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
-    ap.add_argument("--sublayer", choices=["lmhead", "mlp"], default="lmhead",
-                    help="mlp: the chunked SwiGLU-MLP backward (its own JSON line)")
+    ap.add_argument("--sublayer", choices=["lmhead", "mlp", "attn"], default="lmhead",
+                    help="mlp / attn: the chunked SwiGLU-MLP or causal-attention backward (own JSON line)")
     ap.add_argument("--objective", choices=["sft", "grpo", "dpo"], default="sft",
                     help="grpo: 2048-token responses; dpo: 4096-token sequences, both passes per step")
     args = ap.parse_args(argv)
@@ -547,6 +649,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sublayer == "mlp":
         return run_mlp_bench(args)
+    if args.sublayer == "attn":
+        return run_attn_bench(args)
     return run_ours(args)
 
 

@@ -186,6 +186,25 @@ int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, cons
                             void* dX, float* dWgu, float* dWd, int accumulate,
                             void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* Chunked exact backward of causal multi-head self-attention (StreamBP's layer-wise
+ * decomposition with the causal structure: a chunk of queries needs only the keys and
+ * values up to its own position; chatpaper.ai / fugumt.com abstract, atlas.scime.ai
+ * "Approach").  Per head, with scale s: S = s Q K^T (causal), P = exp(S - lse),
+ * D_t = dO_t . O_t, dS = P (dO V^T - D),
+ *     dQ = s dS K,  dK (+)= s dS^T Q,  dV (+)= P^T dO,
+ * computed one chunk of `chunk` queries at a time: chunk [c0, c1) reads keys [0, c1), writes
+ * its dQ rows and adds into dK, dV rows [0, c1).  Only one chunk's P and dS exist at a time.
+ *   Q, K, V, O, dO [H, T, hd] bf16 (head-major); lse [H, T] fp32, the forward's natural
+ *   log-sum-exp of s Q K^T per query row; dQ [H, T, hd] bf16 (overwritten);
+ *   dK, dV [H, T, hd] fp32 (overwritten when accumulate = 0, added to when 1).
+ * hd must be a multiple of 64, at most 256.  Workspace, stream and error rules as for the
+ * LM-head calls. */
+size_t sbp_attn_workspace_bytes(int64_t H, int64_t T, int64_t hd, int64_t chunk);
+int sbp_attn_causal_backward(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                             const float* lse, int64_t H, int64_t T, int64_t hd, float scale, int64_t chunk,
+                             void* dQ, float* dK, float* dV, int accumulate,
+                             void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Size of the fixed scratch array that sbp_lmhead_sft_noalloc works in (bytes). */
 #define SBP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -801,6 +801,149 @@ int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int6
   return SBP_OK;
 }
 
+// ------------------------------------------------------------------ causal attention
+
+// D[z, t] = dO[z, t, :] . O[z, t, :] (one warp per row)
+__global__ void __launch_bounds__(256) k_attn_D(const __nv_bfloat16* __restrict__ O,
+                                                const __nv_bfloat16* __restrict__ dO, int64_t rows, int64_t hd,
+                                                float* __restrict__ D) {
+  const int64_t r = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= rows) return;
+  float acc = 0.f;
+  for (int64_t k = lane; k < hd; k += 32)
+    acc += __bfloat162float(O[r * hd + k]) * __bfloat162float(dO[r * hd + k]);
+  acc = warp_sum(acc);
+  if (lane == 0) D[r] = acc;
+}
+
+// dQ rows of a chunk for every head: sum over the split-K partials [splits][H][rows][hd]
+__global__ void __launch_bounds__(256) k_dq_reduce(const float* __restrict__ part, int splits, int H, int rows,
+                                                   int64_t hd, int64_t T, int64_t c0, __nv_bfloat16* __restrict__ dQ) {
+  const int z = blockIdx.y;
+  const int64_t plane = (int64_t)rows * hd;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < plane; i += (int64_t)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int s2 = 0; s2 < splits; ++s2) acc += part[((int64_t)s2 * H + z) * plane + i];
+    dQ[((int64_t)z * T + c0) * hd + i] = __float2bfloat16_rn(acc);
+  }
+}
+
+struct AttnLayout {
+  int64_t chunk = 0, n_chunks = 0, Cmax = 0, Lp = 0;
+  int splits = 1;
+  size_t off_p = 0, off_ds = 0, off_d = 0, off_dqp = 0, off_cnt = 0, total = 0;
+};
+
+int attn_splits(int64_t rows, int64_t hd, int64_t L, int H) {
+  // dQ units are few (H x row pairs) but long (K = L); split them so that one stays below
+  // a quarter of a pair's share of the launch
+  const int64_t mt_c = (rows + 255) / 256, kb_v = (L + 63) / 64, mt_v = (L + 255) / 256, kb_c = (rows + 63) / 64;
+  const double total = double(H) * double(mt_c * kb_v + mt_v * kb_c);
+  const double per_pair = total / double(std::max(1, num_sms() / 2));
+  int s = (int)std::ceil(4.0 * double(kb_v) / std::max(per_pair, 1.0));
+  s = std::max(1, std::min(s, 8));
+  return (int)std::min<int64_t>(s, kb_v);
+}
+
+bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L) {
+  if (H < 1 || T < 0 || hd < 64 || hd > 256 || hd % 64 || chunk < 1 || chunk > 65535) return false;
+  AttnLayout l;
+  l.chunk = T > 0 ? std::min(chunk, T) : 1;
+  l.n_chunks = T > 0 ? (T + l.chunk - 1) / l.chunk : 0;
+  l.Cmax = ((l.chunk + 255) / 256) * 256;
+  l.Lp = ((std::max<int64_t>(T, 1) + 255) / 256) * 256;
+  l.splits = attn_splits(l.chunk, hd, std::max<int64_t>(T, 1), (int)H);
+  size_t o = 0;
+  l.off_p = o;   o = align256(o + (size_t)H * l.Cmax * l.Lp * 2);
+  l.off_ds = o;  o = align256(o + (size_t)H * l.Cmax * l.Lp * 2);
+  l.off_d = o;   o = align256(o + (size_t)H * std::max<int64_t>(T, 1) * sizeof(float));
+  l.off_dqp = o; o = align256(o + (size_t)l.splits * H * l.Cmax * hd * sizeof(float));
+  l.off_cnt = o; o = align256(o + (size_t)(2 * l.n_chunks + 1) * sizeof(uint32_t));
+  l.total = o;
+  *L = l;
+  return true;
+}
+
+int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
+             int64_t H, int64_t T, int64_t hd, float scale, int64_t chunk, void* dQ, float* dK, float* dV,
+             int accumulate, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s) {
+  AttnLayout L;
+  if (!attn_layout(H, T, hd, chunk, &L)) return SBP_ERR_INVALID_ARG;
+  if (!dev_status || !dK || !dV) return SBP_ERR_INVALID_ARG;
+  if (T > 0 && (!Q || !K || !Vv || !O || !dO || !lse || !dQ)) return SBP_ERR_INVALID_ARG;
+  if (H * T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
+  for (const void* q : {Q, K, Vv, O, dO, (const void*)lse, (const void*)dQ, (const void*)dK, (const void*)dV})
+    if (q && !al16(q)) return SBP_ERR_ALIGNMENT;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return SBP_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  void* pbuf = w + L.off_p;
+  void* dsbuf = w + L.off_ds;
+  float* D = reinterpret_cast<float*>(w + L.off_d);
+  float* dqp = reinterpret_cast<float*>(w + L.off_dqp);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(w + L.off_cnt);
+  int launches = 0;
+  SBP_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
+  SBP_CUDA(cudaMemsetAsync(cnt, 0, (size_t)(2 * L.n_chunks + 1) * sizeof(uint32_t), s));
+  if (!accumulate) {   // every chunk adds into dK and dV rows [0, L)
+    SBP_CUDA(cudaMemsetAsync(dK, 0, (size_t)H * T * hd * sizeof(float), s));
+    SBP_CUDA(cudaMemsetAsync(dV, 0, (size_t)H * T * hd * sizeof(float), s));
+  }
+  if (T == 0) {
+    g_launches = 0;
+    return SBP_OK;
+  }
+  {
+    prof::Scope ps(3, s);
+    k_attn_D<<<(unsigned)((H * T + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(O),
+                                                       static_cast<const __nv_bfloat16*>(dO), H * T, hd, D);
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+  }
+  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+    const int64_t c0 = ci * L.chunk;
+    const int rows = (int)((c0 + L.chunk <= T) ? L.chunk : T - c0);
+    const int64_t Lk = c0 + rows;   // keys of this chunk's queries
+    {
+      prof::Scope ps(0, s);
+      TcAttnArgs a{};
+      a.A = Q; a.B = K; a.T = T; a.hd = hd; a.H = (int)H; a.c0 = c0; a.rows = rows; a.scale = scale;
+      a.lse = lse; a.D = D; a.P = pbuf; a.dS = dsbuf; a.Cmax = L.Cmax; a.Lp = L.Lp; a.status = dev_status;
+      SBP_CUDA(tc_attn(a, false, s));
+      a.A = dO; a.B = Vv;
+      SBP_CUDA(tc_attn(a, true, s));
+      launches += 2;
+    }
+    const int splits = std::min(attn_splits(rows, hd, Lk, (int)H), L.splits);
+    {
+      prof::Scope ps(1, s);
+      // dQ_c = dS K (dH units) and dK[:Lk] += dS^T Q_c (dW units), every head
+      TcBwdArgs b{};
+      b.G = dsbuf; b.ldg = L.Lp; b.g_rows = H * L.Cmax; b.zr_g = (int)L.Cmax;
+      b.W = K; b.w_rows = H * T; b.zr_w = (int)T;
+      b.H = Q; b.h_rows = H * T; b.zr_h = (int)T; b.T = T; b.r0 = c0;
+      b.dW = dK; b.dw_rows = H * T; b.zr_dw = (int)T;
+      b.d = hd; b.V = Lk; b.rows = rows; b.batch = (int)H;
+      b.splits = splits; b.dh_part = dqp; b.dw_accumulate = 1; b.counter = cnt + 2 * ci; b.status = dev_status;
+      SBP_CUDA(tc_backward(b, s));
+      // dV[:Lk] += P^T dO_c (dW units only)
+      TcBwdArgs e = b;
+      e.G = pbuf; e.H = dO; e.dW = dV; e.dw_only = 1; e.counter = cnt + 2 * ci + 1;
+      SBP_CUDA(tc_backward(e, s));
+      launches += 2;
+    }
+    {
+      prof::Scope ps(3, s);
+      dim3 g((unsigned)std::min<int64_t>(((int64_t)rows * hd + 255) / 256, 1024), (unsigned)H);
+      k_dq_reduce<<<g, 256, 0, s>>>(dqp, splits, (int)H, rows, hd, T, c0, static_cast<__nv_bfloat16*>(dQ));
+      ++launches;
+      SBP_CUDA(cudaGetLastError());
+    }
+  }
+  g_launches = launches;
+  return SBP_OK;
+}
+
 }  // namespace
 
 // Scratch of sbp_lmhead_sft_noalloc: a fixed device array in this module, so that
@@ -946,6 +1089,20 @@ int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, cons
                             void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
   return run_mlp(X, Wgu, Wd, dY, T, d, f, chunk, dX, dWgu, dWd, accumulate, workspace, ws_bytes, dev_status,
                  static_cast<cudaStream_t>(stream));
+}
+
+size_t sbp_attn_workspace_bytes(int64_t H, int64_t T, int64_t hd, int64_t chunk) {
+  AttnLayout L;
+  if (!attn_layout(H, T, hd, chunk, &L)) return 0;
+  return L.total;
+}
+
+int sbp_attn_causal_backward(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                             const float* lse, int64_t H, int64_t T, int64_t hd, float scale, int64_t chunk,
+                             void* dQ, float* dK, float* dV, int accumulate, void* workspace, size_t ws_bytes,
+                             int32_t* dev_status, void* stream) {
+  return run_attn(Q, K, V, O, dO, lse, H, T, hd, scale, chunk, dQ, dK, dV, accumulate, workspace, ws_bytes,
+                  dev_status, static_cast<cudaStream_t>(stream));
 }
 
 const char* sbp_status_string(int status) {

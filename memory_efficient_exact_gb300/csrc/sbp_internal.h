@@ -65,6 +65,13 @@ struct TcBwdArgs {
   uint32_t* counter;            // zero before launch
   int32_t* status;
   int dw_only = 0;              // 1: only the dW units (no dH)
+  // a batch of problems stacked along the rows of every operand (attention heads): the
+  // maps span all of them; problem z starts at row z * zr_* of G, W, H and dW, and its
+  // dH partials at plane (split * batch + z)
+  int batch = 1;
+  int zr_g = 0, zr_w = 0, zr_h = 0, zr_dw = 0;
+  // row extents of the maps (0: rows for G, T for H, V for W and dW)
+  int64_t g_rows = 0, w_rows = 0, h_rows = 0, dw_rows = 0;
 };
 cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s);
 
@@ -80,6 +87,20 @@ struct TcMlpArgs {
   int32_t* status;
 };
 cudaError_t tc_mlp(const TcMlpArgs& a, bool da, cudaStream_t s);
+
+// Causal-attention pair GEMMs, sbp_attn.cu, batched over heads.  ds = false: P = softmax
+// row of S = Q_c K^T (lse given) into P; ds = true: dS = s P (dO_c V^T - D) into dS.
+struct TcAttnArgs {
+  const void* A; const void* B;   // Q / K (ds = false) or dO / V (ds = true), [H * T, hd] bf16
+  int64_t T, hd; int H;
+  int64_t c0; int rows;           // queries [c0, c0 + rows), keys [0, c0 + rows)
+  float scale;
+  const float* lse; const float* D;   // [H, T]
+  void* P; void* dS;              // [H, Cmax, Lp] bf16
+  int64_t Cmax, Lp;
+  int32_t* status;
+};
+cudaError_t tc_attn(const TcAttnArgs& a, bool ds, cudaStream_t s);
 
 // SIMT fp32 kernels (fp32 operands), sbp_simt.cu
 cudaError_t simt_forward(const float* H, const float* W, int64_t d, int64_t V, int64_t r0, int rows,

@@ -109,6 +109,11 @@ struct BwdP {
   float* dW; int dw_acc;
   uint32_t* counter;
   int32_t* status; uint64_t limit_ns;
+  // a batch of independent problems (attention heads) stacked along the rows of every
+  // operand: problem z reads G rows from z * zr_g, W rows from z * zr_w, H rows from
+  // z * zr_h and writes dW rows from z * zr_dw (all 0 when batch = 1)
+  int batch, n_dh_b, n_dw_b;
+  int zr_g, zr_w, zr_h, zr_dw;
 };
 
 // k_bwd stages its dW output through shared memory: one 32x32 fp32 block (4 KB, 128-byte
@@ -304,12 +309,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // from the queue and hands it to the peer through distributed shared memory.
 struct Unit {
   int kind, mp, nb, split, kb0, kb1;
+  int z;   // problem of the batch
 };
 
 __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
   Unit w;
   if (u < p.n_dh) {
     w.kind = 0;
+    w.z = u / p.n_dh_b;
+    u -= w.z * p.n_dh_b;
     w.mp = u % p.mt_c;
     w.nb = (u / p.mt_c) % p.nt_d;
     w.split = u / (p.mt_c * p.nt_d);
@@ -318,6 +326,8 @@ __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
   } else {
     u -= p.n_dh;
     w.kind = 1;
+    w.z = u / p.n_dw_b;
+    u -= w.z * p.n_dw_b;
     w.nb = u % p.nt_d;
     w.mp = u / p.nt_d;
     w.split = 0;
@@ -379,15 +389,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t fb = mapa(saddr(&c->full[stage]), 0);
           if (rank == 0) mbar_expect_tx(&c->full[stage], PAIR_TX);
           if (w.kind == 0) {
-            tma_load_2d_pair(sa, &tmGk, fb, kb * BK, mrow);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) tma_load_2d_pair(sb + j * BOX_BYTES, &tmWmn, fb, ncol + j * 64, kb * BK);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) tma_load_2d_pair(sa + j * BOX_BYTES, &tmGmn, fb, mrow + j * 64, kb * BK);
+            tma_load_2d_pair(sa, &tmGk, fb, kb * BK, w.z * p.zr_g + mrow);
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(sb + j * BOX_BYTES, &tmHmn, fb, ncol + j * 64, (int)(p.r0 + (int64_t)kb * BK));
+              tma_load_2d_pair(sb + j * BOX_BYTES, &tmWmn, fb, ncol + j * 64, w.z * p.zr_w + kb * BK);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(sa + j * BOX_BYTES, &tmGmn, fb, mrow + j * 64, w.z * p.zr_g + kb * BK);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(sb + j * BOX_BYTES, &tmHmn, fb, ncol + j * 64,
+                               (int)(w.z * (int64_t)p.zr_h + p.r0 + (int64_t)kb * BK));
           }
           issued |= 1u << stage;
           last_phase[stage] = phase;
@@ -474,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool vrow;
       if (w.kind == 0) {
         vrow = row < p.rows;
-        dst = p.dh_part + (int64_t)w.split * p.plane + row * p.d;
+        dst = p.dh_part + ((int64_t)w.split * p.batch + w.z) * p.plane + row * p.d;
       } else {
         vrow = row < p.V;
         dst = p.dW + row * p.d;
@@ -507,8 +520,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async();
           __syncwarp();
           if (lane == 0 && y0 < p.V) {
-            if (p.dw_acc) tma_reduce_add_2d(&tmDW, stg, (int)cg, y0);
-            else tma_store_2d(&tmDW, stg, (int)cg, y0);
+            const int yz = w.z * p.zr_dw + y0;
+            if (p.dw_acc) tma_reduce_add_2d(&tmDW, stg, (int)cg, yz);
+            else tma_store_2d(&tmDW, stg, (int)cg, yz);
             bulk_commit();
           }
         }
@@ -588,12 +602,16 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   if (!set_smem_attr()) return cudaErrorInvalidConfiguration;
   CUtensorMap mGk, mGmn, mWmn, mHmn;
   // G: [rows, V] with row stride ldg; rows past the chunk read as zero.
-  if (!make_map(&mGk, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, BK, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mGmn, a.G, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&mWmn, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&mHmn, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  const uint64_t g_rows = a.g_rows ? (uint64_t)a.g_rows : (uint64_t)a.rows;
+  const uint64_t w_rows = a.w_rows ? (uint64_t)a.w_rows : (uint64_t)a.V;
+  const uint64_t h_rows = a.h_rows ? (uint64_t)a.h_rows : (uint64_t)a.T;
+  const uint64_t dw_rows = a.dw_rows ? (uint64_t)a.dw_rows : (uint64_t)a.V;
+  if (!make_map(&mGk, a.G, (uint64_t)a.V, g_rows, (uint64_t)a.ldg, BK, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mGmn, a.G, (uint64_t)a.V, g_rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&mWmn, a.W, (uint64_t)a.d, w_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&mHmn, a.H, (uint64_t)a.d, h_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap mDW;
-  if (!make_map_f32(&mDW, a.dW, (uint64_t)a.d, (uint64_t)a.V)) return cudaErrorInvalidValue;
+  if (!make_map_f32(&mDW, a.dW, (uint64_t)a.d, dw_rows)) return cudaErrorInvalidValue;
   BwdP p;
   p.rows = a.rows; p.r0 = a.r0; p.V = a.V; p.d = a.d;
   p.mt_c = (a.rows + 255) / 256;
@@ -602,8 +620,12 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   p.splits = a.splits;
   p.mt_v = (int)((a.V + 255) / 256);
   p.kb_c = (a.rows + BK - 1) / BK;
-  p.n_dh = a.dw_only ? 0 : p.mt_c * p.nt_d * p.splits;
-  p.n_total = p.n_dh + p.mt_v * p.nt_d;
+  p.batch = a.batch > 0 ? a.batch : 1;
+  p.n_dh_b = a.dw_only ? 0 : p.mt_c * p.nt_d * p.splits;
+  p.n_dw_b = p.mt_v * p.nt_d;
+  p.n_dh = p.n_dh_b * p.batch;
+  p.n_total = p.n_dh + p.n_dw_b * p.batch;
+  p.zr_g = a.zr_g; p.zr_w = a.zr_w; p.zr_h = a.zr_h; p.zr_dw = a.zr_dw;
   p.dh_part = a.dh_part; p.plane = (int64_t)a.rows * a.d;
   p.dW = a.dW; p.dw_acc = a.dw_accumulate;
   p.counter = a.counter; p.status = a.status; p.limit_ns = wait_limit_ns();

@@ -59,6 +59,10 @@ def _load() -> ctypes.CDLL:
     lib.sbp_mlp_workspace_bytes.argtypes = [I64, I64, I64, I64]
     lib.sbp_mlp_swiglu_backward.restype = C
     lib.sbp_mlp_swiglu_backward.argtypes = [P, P, P, P, I64, I64, I64, I64, P, P, P, C, P, SZ, P, P]
+    lib.sbp_attn_workspace_bytes.restype = SZ
+    lib.sbp_attn_workspace_bytes.argtypes = [I64, I64, I64, I64]
+    lib.sbp_attn_causal_backward.restype = C
+    lib.sbp_attn_causal_backward.argtypes = [P, P, P, P, P, P, I64, I64, I64, F, I64, P, P, P, C, P, SZ, P, P]
     lib.sbp_status_string.restype = ctypes.c_char_p
     lib.sbp_status_string.argtypes = [C]
     lib.sbp_last_launch_count.restype = C
@@ -328,3 +332,36 @@ def mlp_swiglu_backward(X, Wgu, Wd, dY, chunk, *, dX=None, dWgu=None, dWd=None, 
                                         int(bool(accumulate)), _p(workspace), workspace.numel(), _p(st),
                                         _stream(stream)), "sbp_mlp_swiglu_backward")
     return dict(dX=dX, dWgu=dWgu, dWd=dWd, status=st)
+
+
+def attn_workspace_bytes(H: int, T: int, hd: int, chunk: int) -> int:
+    return int(_lib.sbp_attn_workspace_bytes(H, T, hd, chunk))
+
+
+def attn_causal_backward(Q, K, V, O, dO, lse, scale, chunk, *, dQ=None, dK=None, dV=None, accumulate=False,
+                         workspace=None, status=None, stream=None) -> dict:
+    """Chunked causal-attention backward (``sbp_attn_causal_backward``).
+
+    Q, K, V, O, dO [H, T, hd] bf16; lse [H, T] fp32 (the forward's row log-sum-exp)."""
+    _dev(Q, K, V, O, dO, lse)
+    H, T, hd = Q.shape
+    for t in (K, V, O, dO):
+        if t.shape != (H, T, hd) or t.dtype != torch.bfloat16:
+            raise ValueError("Q, K, V, O, dO must be bf16 [H, T, hd]")
+    if Q.dtype != torch.bfloat16 or lse.shape != (H, T) or lse.dtype != torch.float32:
+        raise ValueError("Q bf16 [H, T, hd]; lse fp32 [H, T]")
+    dev = Q.device
+    if workspace is None:
+        n = attn_workspace_bytes(H, T, hd, chunk)
+        if n == 0:
+            raise SbpError(ERR_INVALID_ARG, "attn_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty((H, T, hd), dtype=torch.float32, device=dev) if dK is None else dK
+    dV = torch.empty((H, T, hd), dtype=torch.float32, device=dev) if dV is None else dV
+    _dev(dQ, dK, dV)
+    st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
+    _check(_lib.sbp_attn_causal_backward(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(lse), H, T, hd, float(scale), chunk,
+                                         _p(dQ), _p(dK), _p(dV), int(bool(accumulate)), _p(workspace),
+                                         workspace.numel(), _p(st), _stream(stream)), "sbp_attn_causal_backward")
+    return dict(dQ=dQ, dK=dK, dV=dV, status=st)
