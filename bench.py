@@ -543,6 +543,8 @@ def run_attn_bench(args):
         w["chunk"] = args.chunk
     if args.tokens:
         w["T"] = args.tokens
+    if args.hd:
+        w["hd"] = args.hd
     H, T, hd, chunk = w["H"], w["T"], w["hd"], w["chunk"]
     dev = torch.device("cuda", torch.cuda.current_device())
     g = torch.Generator(device=dev).manual_seed(w["seed"])
@@ -586,23 +588,31 @@ def run_attn_bench(args):
     # L = the chunk's keys; the causal upper triangle of the diagonal block is included
     rowkeys = sum(min(chunk, T - c0) * min(T, c0 + chunk) for c0 in range(0, T, chunk))
     flops = 5 * 2 * hd * H * rowkeys
+    fused = hd == 128   # P and dS stay on chip (k_attn_kv, k_attn_q); else chunk buffers in HBM
     # chunk buffers: P and dS written once and read twice each (2 bytes an element)
-    pds_bytes = 12 * H * rowkeys
+    pds_bytes = 0 if fused else 12 * H * rowkeys
     sp_ms, sp_n = prof["forward_gemm"]
     bw_ms, bw_n = prof["backward_gemm"]
+    if fused:   # k_attn_kv forms S, dP and accumulates dV, dK; k_attn_q forms S, dP and accumulates dQ
+        names, gemms = ("k_attn_kv (S, dP, dV, dK)", "k_attn_q (S, dP, dQ)"), (4, 3)
+    else:
+        names, gemms = ("k_attn (P, dS)", "k_bwd (dQ + dK, dV)"), (2, 3)
     line = {
-        "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "metric": ATTN_METRIC if (H, T, hd) == (32, 8192, 128) else f"attention bwd tokens/s (causal, H={H}, hd={hd}, T={T})",
+        "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"causal_attn_bwd_bf16_H{H}_T{T}_hd{hd}_chunk{chunk}", "H": H, "T": T, "hd": hd,
                    "chunk": chunk},
         "executed_tflops": flops * args.steps / (ms / 1000.0) / 1e12,
         "pct_bf16_peak": 100.0 * flops * args.steps / (ms / 1000.0) / 1e12 / peaks["bf16_tflops"],
-        "chunk_buffer_gbs": pds_bytes * args.steps / (ms / 1000.0) / 1e9,
-        "kernels": {"k_attn (P, dS)": {"ms": sp_ms, "launches": sp_n,
-                                      "tflops": 4 * hd * H * rowkeys * args.steps / (sp_ms / 1000.0) / 1e12 if sp_n else None},
-                    "k_bwd (dQ + dK, dV)": {"ms": bw_ms, "launches": bw_n,
-                                            "tflops": 6 * hd * H * rowkeys * args.steps / (bw_ms / 1000.0) / 1e12 if bw_n else None},
+        "chunk_buffer_gbs": pds_bytes * args.steps / (ms / 1000.0) / 1e9 if pds_bytes else None,
+        "kernels": {names[0]: {"ms": sp_ms, "launches": sp_n,
+                               "tflops": 2 * gemms[0] * hd * H * rowkeys * args.steps / (sp_ms / 1000.0) / 1e12
+                               if sp_n else None},
+                    names[1]: {"ms": bw_ms, "launches": bw_n,
+                               "tflops": 2 * gemms[1] * hd * H * rowkeys * args.steps / (bw_ms / 1000.0) / 1e12
+                               if bw_n else None},
                     "other": {"ms": prof["other"][0], "launches": prof["other"][1]}},
         "peak_source": src, "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
         "unchunked_scores_gb": H * T * T * 2 * 2 / 1e9,
@@ -623,6 +633,7 @@ def main(argv=None):
                     help="profile: a small case of the same kernels for ncu captures")
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
+    ap.add_argument("--hd", type=int, default=None, help="override the attention head width (--sublayer attn)")
     ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
     ap.add_argument("--sublayer", choices=["lmhead", "mlp", "attn"], default="lmhead",
                     help="mlp / attn: the chunked SwiGLU-MLP or causal-attention backward (own JSON line)")

@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsbp.so")
-SOURCES = ["sbp_api.cu", "sbp_simt.cu", "sbp_tc.cu", "sbp_mlp.cu", "sbp_attn.cu"]
+SOURCES = ["sbp_api.cu", "sbp_simt.cu", "sbp_tc.cu", "sbp_mlp.cu", "sbp_attn.cu", "sbp_attn_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include"),
          "--expt-relaxed-constexpr"]

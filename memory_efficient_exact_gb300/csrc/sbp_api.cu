@@ -832,6 +832,7 @@ __global__ void __launch_bounds__(256) k_dq_reduce(const float* __restrict__ par
 struct AttnLayout {
   int64_t chunk = 0, n_chunks = 0, Cmax = 0, Lp = 0;
   int splits = 1;
+  bool fused = false;   // hd = 128: P and dS stay on chip, the workspace holds D only
   size_t off_p = 0, off_ds = 0, off_d = 0, off_dqp = 0, off_cnt = 0, total = 0;
 };
 
@@ -854,7 +855,14 @@ bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L)
   l.Cmax = ((l.chunk + 255) / 256) * 256;
   l.Lp = ((std::max<int64_t>(T, 1) + 255) / 256) * 256;
   l.splits = attn_splits(l.chunk, hd, std::max<int64_t>(T, 1), (int)H);
+  l.fused = hd == 128;
   size_t o = 0;
+  if (l.fused) {
+    l.off_d = o; o = align256(o + (size_t)H * std::max<int64_t>(T, 1) * sizeof(float));
+    l.total = o;
+    *L = l;
+    return true;
+  }
   l.off_p = o;   o = align256(o + (size_t)H * l.Cmax * l.Lp * 2);
   l.off_ds = o;  o = align256(o + (size_t)H * l.Cmax * l.Lp * 2);
   l.off_d = o;   o = align256(o + (size_t)H * std::max<int64_t>(T, 1) * sizeof(float));
@@ -863,6 +871,48 @@ bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L)
   l.total = o;
   *L = l;
   return true;
+}
+
+// hd = 128: per chunk, k_attn_kv (dK, dV of keys [0, c1)) then k_attn_q (dQ of the chunk)
+int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
+                   int64_t H, int64_t T, float scale, const AttnLayout& L, void* dQ, float* dK, float* dV,
+                   int accumulate, char* w, int32_t* dev_status, cudaStream_t s) {
+  const int64_t hd = 128;
+  float* D = reinterpret_cast<float*>(w + L.off_d);
+  int launches = 0;
+  SBP_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
+  if (!accumulate) {
+    SBP_CUDA(cudaMemsetAsync(dK, 0, (size_t)H * T * hd * sizeof(float), s));
+    SBP_CUDA(cudaMemsetAsync(dV, 0, (size_t)H * T * hd * sizeof(float), s));
+  }
+  if (T == 0) {
+    g_launches = 0;
+    return SBP_OK;
+  }
+  AttnFusedPlan plan;
+  if (!plan.init(Q, K, Vv, dO, dK, dV, T, H)) return SBP_ERR_CUDA;
+  {
+    prof::Scope ps(3, s);
+    k_attn_D<<<(unsigned)((H * T + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(O),
+                                                       static_cast<const __nv_bfloat16*>(dO), H * T, hd, D);
+    ++launches;
+    SBP_CUDA(cudaGetLastError());
+  }
+  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+    const int64_t c0 = ci * L.chunk, c1 = std::min(T, c0 + L.chunk);
+    {
+      prof::Scope ps(0, s);
+      SBP_CUDA(attn_fused_kv(plan, c0, c1, scale, lse, D, dev_status, s));
+      ++launches;
+    }
+    {
+      prof::Scope ps(1, s);
+      SBP_CUDA(attn_fused_q(plan, c0, c1, scale, lse, D, dQ, dev_status, s));
+      ++launches;
+    }
+  }
+  g_launches = launches;
+  return SBP_OK;
 }
 
 int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
@@ -877,6 +927,7 @@ int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const 
     if (q && !al16(q)) return SBP_ERR_ALIGNMENT;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return SBP_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
+  if (L.fused) return run_attn_fused(Q, K, Vv, O, dO, lse, H, T, scale, L, dQ, dK, dV, accumulate, w, dev_status, s);
   void* pbuf = w + L.off_p;
   void* dsbuf = w + L.off_ds;
   float* D = reinterpret_cast<float*>(w + L.off_d);

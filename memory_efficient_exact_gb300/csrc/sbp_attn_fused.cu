@@ -1,0 +1,847 @@
+// Fused tensor-core kernels of the chunked causal-attention backward at head dimension
+// 128 (bf16 operands, fp32 accumulation, sm_103a).
+//
+// Per chunk of queries [c0, c1), which reads keys [0, c1) only (the causal structure
+// StreamBP uses), two SM-pair kernels keep the chunk's probabilities and score gradients
+// on chip: nothing of size (queries x keys) goes through HBM.
+//
+//   k_attn_kv  unit = (head, 256 keys).  dV and dK of those keys stay in tensor memory
+//              while the unit walks the chunk's query blocks of 128:
+//                S^T = K Q^T,  dP^T = V dO^T                      (tensor memory)
+//                P^T = exp(s S^T - lse),  dS^T = P^T (dP^T - D)   (epilogue -> shared memory)
+//                dV += P^T dO,  dK += dS^T Q                      (tensor memory)
+//              then adds dV and s dK into the fp32 outputs (TMA reduce-add).
+//   k_attn_q   unit = (head, 256 queries of the chunk).  dQ stays in tensor memory while
+//              the unit walks the key blocks of 128 up to its last query:
+//                S = Q K^T,  dP = dO V^T,  dS = P (dP - D),  dQ += dS K
+//              then stores s dQ in bf16.
+// S and dP are formed in both kernels, so that no accumulator is shared between units:
+// every output element is written by one unit in a fixed order (deterministic, no
+// floating-point atomics).
+//
+// Pair protocol as in the other tensor-core kernels: the leader CTA's thread issues
+// tcgen05.mma cta_group::2 with M = 256 (128 rows in each CTA) and N = 128 (each CTA
+// supplies half of B); TMA copies of both CTAs complete on the leader's barriers; the
+// commits are multicast to both CTAs; every wait is bounded in time.
+#include "sbp_tc_common.cuh"
+
+namespace sbp {
+namespace tc {
+namespace fa {
+
+constexpr int KV_THREADS = NUM_THREADS + 32;  // + one warp that stages lse and D per block
+constexpr uint32_t IDESC_KK = idesc_bf16(256, 128, false, false);  // A, B K-major
+constexpr uint32_t IDESC_KM = idesc_bf16(256, 128, false, true);   // A K-major, B MN-major
+
+// Shared memory of k_attn_kv, bytes from the 1024-aligned base.  Tiles are 128-byte
+// swizzled: [64-element block][rows][128 B].
+constexpr uint32_t KV_K = 0;          // K rows of the unit (this CTA's 128 keys x 128)
+constexpr uint32_t KV_V = 32768;      // V rows
+constexpr uint32_t KV_A = 65536;      // 2 stages: Q then dO of the block, this CTA's 64 queries x 128
+constexpr uint32_t KV_A_STAGE = 32768;
+constexpr uint32_t KV_B = 131072;     // Q then dO of the block, 128 queries x this CTA's 64 of hd
+constexpr uint32_t KV_PT = 163840;    // P^T  [2 query halves][128 keys][128 B]
+constexpr uint32_t KV_DST = 196608;   // dS^T [2 query halves][128 keys][128 B]
+constexpr uint32_t KV_LD = 229376;    // lse * log2(e) [128], then D [128], of the block's queries
+constexpr uint32_t KV_CTRL = 230400;
+
+// Shared memory of k_attn_q.
+constexpr uint32_t Q_Q = 0;           // Q rows of the unit (this CTA's 128 queries x 128)
+constexpr uint32_t Q_DO = 32768;      // dO rows
+constexpr uint32_t Q_X = 65536;       // 2 stages: K then V of the key block, this CTA's 64 keys x 128
+constexpr uint32_t Q_X_STAGE = 32768;
+constexpr uint32_t Q_Y = 131072;      // 2 stages: K of the key block, 128 keys x this CTA's 64 of hd
+constexpr uint32_t Q_Y_STAGE = 16384;
+constexpr uint32_t Q_DS = 163840;     // dS [2 key halves][128 queries][128 B]
+constexpr uint32_t Q_CTRL = 196608;
+
+struct CtrlF {
+  uint64_t afull[2], aempty[2];  // ring of the S / dP B operands
+  uint64_t bfull[2], bempty[2];  // ring of the B operands of the accumulating GEMMs
+  uint64_t rfull, rempty;        // the unit's resident A operands
+  uint64_t tfull, tempty;        // S and dP accumulators
+  uint64_t oready, ofree;        // P^T, dS^T (or dS) in shared memory
+  uint64_t accempty;             // the unit's accumulators have been read out
+  uint64_t lfull, lempty;        // lse / D of the block (k_attn_kv)
+  uint64_t sfree;                // the dV / dK staging has left shared memory (k_attn_kv)
+  uint64_t mdone;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t SMEM_KV = KV_CTRL + sizeof(CtrlF) + 1024;
+constexpr size_t SMEM_Q = Q_CTRL + sizeof(CtrlF) + 1024;
+static_assert(SMEM_KV <= 232448, "k_attn_kv shared memory");
+
+__device__ __forceinline__ void prologue_f(CtrlF* c, int warp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->afull[i], 1);
+      mbar_init(&c->aempty[i], 1);
+      mbar_init(&c->bfull[i], 1);
+      mbar_init(&c->bempty[i], 1);
+    }
+    mbar_init(&c->rfull, 1);
+    mbar_init(&c->rempty, 1);
+    mbar_init(&c->tfull, 1);
+    mbar_init(&c->tempty, 2 * NUM_EPI_WARPS);
+    mbar_init(&c->oready, 2 * NUM_EPI_WARPS);
+    mbar_init(&c->ofree, 1);
+    mbar_init(&c->accempty, 2 * NUM_EPI_WARPS);
+    mbar_init(&c->lfull, 1);
+    mbar_init(&c->lempty, NUM_EPI_WARPS);
+    mbar_init(&c->sfree, NUM_EPI_WARPS);
+    mbar_init(&c->mdone, 1);
+    c->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&c->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+}
+
+__device__ __forceinline__ void teardown_f(CtrlF* c, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(c->tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ void fail_f(CtrlF* c, int32_t* status) {
+  *(volatile int*)&c->abort = 1;
+  if (status) atomicCAS(status, 0, SBP_ERR_TIMEOUT);
+}
+
+// Waits until barrier b has completed `need` phases; `seen` counts the phases this
+// thread already waited for.  Bounded like every other wait.
+__device__ __forceinline__ bool wait_n(uint64_t* b, uint32_t& seen, uint32_t need, CtrlF* c, uint64_t limit) {
+  while (seen < need) {
+    if (!wait_cluster(b, seen & 1u, &c->abort, limit)) return false;
+    ++seen;
+  }
+  return true;
+}
+// The same for a whole warp (seen and need are warp-uniform).
+__device__ __forceinline__ bool warp_wait_n(uint64_t* b, uint32_t& seen, uint32_t need, CtrlF* c, uint64_t limit) {
+  while (seen < need) {
+    if (!__all_sync(0xffffffffu, wait_cluster(b, seen & 1u, &c->abort, limit))) return false;
+    ++seen;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar_cluster, int x,
+                                                 int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Row `row` (128 B = 64 bf16) of a 128-byte-swizzled K-major tile: 16-byte chunk k at
+// chunk k ^ (row % 8), the layout TMA writes and tcgen05.mma reads.
+__device__ __forceinline__ void store_row128(uint32_t tile, int row, const uint32_t (&w)[32]) {
+  const uint32_t r = tile + (uint32_t)row * 128u;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    sts128(r + ((uint32_t)(k ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+// ================================================================ k_attn_kv (dK, dV)
+
+struct KvP {
+  int H, T, c0, c1, nb, n_units;
+  float scale;
+  const float* lse;  // [H, T]
+  const float* D;    // [H, T]
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
+// Unit u: head z, keys [256 kp, 256 kp + 256); query blocks b0 .. nb-1 of the chunk hold
+// at least one query at or after the unit's first key.  Key pairs in ascending order, so
+// the longest units start first.
+__device__ __forceinline__ void kv_unit(const KvP& p, int u, int& z, int& kp, int& b0) {
+  kp = u / p.H;
+  z = u - kp * p.H;
+  const int num = 256 * kp - p.c0 - 127;
+  b0 = num <= 0 ? 0 : (num + 127) / 128;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
+    k_attn_kv(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const __grid_constant__ CUtensorMap tmQa, const __grid_constant__ CUtensorMap tmOa,
+              const __grid_constant__ CUtensorMap tmQb, const __grid_constant__ CUtensorMap tmOb,
+              const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV, const KvP p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  CtrlF* c = reinterpret_cast<CtrlF*>(base + KV_CTRL);
+  const uint32_t sb = saddr(base);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ctarank();
+  prologue_f(c, warp);
+  const uint32_t tmem = c->tmem_base;
+  const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // the unit's K and V, then ring A: Q and dO of each block (this CTA's 64 queries)
+      prefetch_map(&tmK);
+      prefetch_map(&tmV);
+      prefetch_map(&tmQa);
+      prefetch_map(&tmOa);
+      int sa = 0;
+      uint32_t pha = 0, phr = 0, iss = 0, lph_a[2] = {0, 0}, lph_r = 0;
+      bool ok = true;
+      for (int u = pid; u < p.n_units && ok; u += npairs) {
+        int z, kp, b0;
+        kv_unit(p, u, z, kp, b0);
+        if (!wait_bounded(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        const uint32_t fr = mapa(saddr(&c->rfull), 0);
+        if (rank == 0) mbar_expect_tx(&c->rfull, 4u * 32768u);
+        const int krow = 256 * kp + 128 * (int)rank;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          tma_load_3d_pair(sb + KV_K + hb * 16384, &tmK, fr, 64 * hb, krow, z);
+          tma_load_3d_pair(sb + KV_V + hb * 16384, &tmV, fr, 64 * hb, krow, z);
+        }
+        iss |= 4u;
+        lph_r = phr;
+        phr ^= 1u;
+        for (int b = b0; b < p.nb; ++b) {
+          if (!wait_bounded(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t fa = mapa(saddr(&c->afull[sa]), 0);
+          if (rank == 0) mbar_expect_tx(&c->afull[sa], 2u * KV_A_STAGE);
+          const uint32_t st = sb + KV_A + sa * KV_A_STAGE;
+          const int qrow = p.c0 + 128 * b + 64 * (int)rank;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            tma_load_3d_pair(st + hb * 8192, &tmQa, fa, 64 * hb, qrow, z);
+            tma_load_3d_pair(st + 16384 + hb * 8192, &tmOa, fa, 64 * hb, qrow, z);
+          }
+          iss |= 1u << sa;
+          lph_a[sa] = pha;
+          if (++sa == 2) { sa = 0; pha ^= 1u; }
+        }
+      }
+      if (!ok) {
+        fail_f(c, p.status);
+        if (rank == 0) {
+          if (iss & 4u) wait_bounded(&c->rfull, lph_r, nullptr, 200000000ull);
+          for (int s = 0; s < 2; ++s)
+            if (iss & (1u << s)) wait_bounded(&c->afull[s], lph_a[s], nullptr, 200000000ull);
+        }
+      }
+    } else if (lane == 16) {
+      // ring B (one stage): Q and dO of the block, 128 queries x this CTA's half of hd
+      prefetch_map(&tmQb);
+      prefetch_map(&tmOb);
+      uint32_t phb = 0, lph = 0;
+      bool ok = true, any = false;
+      for (int u = pid; u < p.n_units && ok; u += npairs) {
+        int z, kp, b0;
+        kv_unit(p, u, z, kp, b0);
+        for (int b = b0; b < p.nb; ++b) {
+          if (!wait_bounded(&c->bempty[0], phb ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t fb = mapa(saddr(&c->bfull[0]), 0);
+          if (rank == 0) mbar_expect_tx(&c->bfull[0], 4u * 16384u);
+          const int qrow = p.c0 + 128 * b;
+          tma_load_3d_pair(sb + KV_B, &tmQb, fb, 64 * (int)rank, qrow, z);
+          tma_load_3d_pair(sb + KV_B + 16384, &tmOb, fb, 64 * (int)rank, qrow, z);
+          any = true;
+          lph = phb;
+          phb ^= 1u;
+        }
+      }
+      if (!ok) {
+        fail_f(c, p.status);
+        if (rank == 0 && any) wait_bounded(&c->bfull[0], lph, nullptr, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      int sa = 0, lu = 0;
+      uint32_t pha = 0, phb = 0, phr = 0, tempty_seen = 0, oready_seen = 0, acc_seen = 0, g = 0;
+      bool ok = true;
+      // dV += P^T dO and dK += dS^T Q for global block gg (the first of its unit overwrites)
+      auto accumulate = [&](uint32_t gg, bool first) -> bool {
+        if (!wait_n(&c->oready, oready_seen, gg + 1, c, p.limit_ns)) return false;
+        if (!wait_bounded(&c->bfull[0], phb, &c->abort, p.limit_ns)) return false;
+        phb ^= 1u;
+        if (first && !wait_n(&c->accempty, acc_seen, (uint32_t)lu, c, p.limit_ns)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma2_bf16(tmem + 256, sw128_desc(sb + KV_PT + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                    sw128_desc(sb + KV_B + 16384 + k * 2048, 16384, 1024), IDESC_KM, (!first || k) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma2_bf16(tmem + 384, sw128_desc(sb + KV_DST + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                    sw128_desc(sb + KV_B + k * 2048, 16384, 1024), IDESC_KM, (!first || k) ? 1u : 0u);
+        commit2_mc(&c->bempty[0], 3);
+        commit2_mc(&c->ofree, 3);
+        return true;
+      };
+      for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
+        int z, kp, b0;
+        kv_unit(p, u, z, kp, b0);
+        const int nbl = p.nb - b0;
+        if (!wait_bounded(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
+        phr ^= 1u;
+        tc_fence_after();
+        for (int n = 0; n < nbl; ++n, ++g) {
+          // S^T and dP^T of block g; the previous block's accumulation follows, so the
+          // epilogue's work on block g overlaps it
+          if (!wait_n(&c->tempty, tempty_seen, g, c, p.limit_ns)) { ok = false; break; }
+          if (!wait_bounded(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = sb + KV_A + sa * KV_A_STAGE;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma2_bf16(tmem, sw128_desc(sb + KV_K + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                      sw128_desc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma2_bf16(tmem + 128, sw128_desc(sb + KV_V + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                      sw128_desc(st + 16384 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+          commit2_mc(&c->aempty[sa], 3);
+          commit2_mc(&c->tfull, 3);
+          if (n == nbl - 1) commit2_mc(&c->rempty, 3);
+          if (++sa == 2) { sa = 0; pha ^= 1u; }
+          if (n >= 1 && !accumulate(g - 1, n == 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!accumulate(g - 1, nbl == 1)) { ok = false; break; }
+      }
+      if (!ok) fail_f(c, p.status);
+      commit2_mc(&c->mdone, 1);
+      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp == NUM_EPI_WARPS + 2) {
+    // lse * log2(e) and D of each block's 128 queries into shared memory (one buffer,
+    // refilled once the 8 epilogue warps have read it); loads issued a block ahead
+    float* ld = reinterpret_cast<float*>(base + KV_LD);
+    uint32_t lempty_seen = 0, g = 0;
+    for (int u = pid; u < p.n_units; u += npairs) {
+      int z, kp, b0;
+      kv_unit(p, u, z, kp, b0);
+      bool ok = true;
+      for (int b = b0; b < p.nb; ++b, ++g) {
+        float lv[4], dv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = p.c0 + 128 * b + lane + 32 * i;
+          const bool v = q < p.c1;
+          const int64_t o = (int64_t)z * p.T + q;
+          lv[i] = v ? p.lse[o] * L2E : 0.f;
+          dv[i] = v ? p.D[o] : 0.f;
+        }
+        if (!warp_wait_n(&c->lempty, lempty_seen, g, c, p.limit_ns)) { ok = false; break; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ld[lane + 32 * i] = lv[i];
+          ld[128 + lane + 32 * i] = dv[i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->lfull);
+      }
+      if (!ok) {
+        fail_f(c, p.status);
+        break;
+      }
+    }
+  } else {
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int lrow = q * 32 + lane;
+    const uint32_t trow = (uint32_t)(q * 32) << 16;
+    const float sl2 = p.scale * L2E;
+    const float* ld = reinterpret_cast<const float*>(base + KV_LD);
+    uint32_t tfull_seen = 0, ofree_seen = 0, lfull_seen = 0, sfree_seen = 0, g = 0;
+    int lu = 0;
+    bool ok = true;
+    for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
+      int z, kp, b0;
+      kv_unit(p, u, z, kp, b0);
+      const int kw = 256 * kp + 128 * (int)rank + 32 * q;   // this warp's first key
+      const int key = kw + lane;
+      for (int b = b0; b < p.nb; ++b, ++g) {
+        if (!warp_wait_n(&c->tfull, tfull_seen, g + 1, c, p.limit_ns) ||
+            !warp_wait_n(&c->lfull, lfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pw[32], dw[32];   // bf16 pairs of P^T and dS^T over this thread's 64 queries
+#pragma unroll
+        for (int gq = 0; gq < 2; ++gq) {
+          uint32_t rs[32], rd[32];
+          tmem_ld32(tmem + trow + (uint32_t)(64 * h + 32 * gq), rs);
+          tmem_ld32(tmem + trow + (uint32_t)(128 + 64 * h + 32 * gq), rd);
+          tmem_ld_wait();
+          if (gq == 1) {   // S^T and dP^T are in registers: the next block's may be formed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_cluster(mapa(saddr(&c->tempty), 0));
+          }
+          const int qg = p.c0 + 128 * b + 64 * h + 32 * gq;   // first query of the group
+          const bool none = qg + 31 < kw || qg >= p.c1;
+          const bool all = qg >= kw + 31 && qg + 31 < p.c1;
+          if (none) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pw[16 * gq + j] = dw[16 * gq + j] = 0u;
+            continue;
+          }
+          const float4* l4 = reinterpret_cast<const float4*>(ld + 64 * h + 32 * gq);
+          const float4* d4 = reinterpret_cast<const float4*>(ld + 128 + 64 * h + 32 * gq);
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 L = l4[j4], Dv = d4[j4];
+            const float lz[4] = {L.x, L.y, L.z, L.w}, dz[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+            float pv[4], sv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * j4 + e;
+              float pe = ex2(fmaf(__uint_as_float(rs[j]), sl2, -lz[e]));
+              if (!all && (qg + j < key || qg + j >= p.c1)) pe = 0.f;
+              pv[e] = pe;
+              sv[e] = pe * (__uint_as_float(rd[j]) - dz[e]);
+            }
+            pw[16 * gq + 2 * j4] = pack_bf16(pv[0], pv[1]);
+            pw[16 * gq + 2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
+            dw[16 * gq + 2 * j4] = pack_bf16(sv[0], sv[1]);
+            dw[16 * gq + 2 * j4 + 1] = pack_bf16(sv[2], sv[3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->lempty);
+        // the previous block's accumulation has read P^T and dS^T; at a unit's first
+        // block, also the previous unit's dV / dK staging has left this area
+        if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns) ||
+            (b == b0 && !warp_wait_n(&c->sfree, sfree_seen, (uint32_t)lu, c, p.limit_ns))) { ok = false; break; }
+        store_row128(sb + KV_PT + h * 16384, lrow, pw);
+        store_row128(sb + KV_DST + h * 16384, lrow, dw);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) arrive_cluster(mapa(saddr(&c->oready), 0));
+      }
+      if (!ok) break;
+      // the unit's dV and dK: out of tensor memory, through this warp's 8 KB of the
+      // P^T / dS^T area, added into the fp32 outputs.  Each output element receives one
+      // add per launch; rows past T are clipped by the tensor map, rows in [c1, T) add 0.
+      if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t stg = sb + KV_PT + (uint32_t)(warp - 2) * 8192u;
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {   // t = 0: dV, t = 1: s dK
+        uint32_t ra[2][32];
+        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 64 * h), ra[0]);
+        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 64 * h + 32), ra[1]);
+        tmem_ld_wait();
+        if (t == 1) {   // both accumulators are in registers: the next unit may overwrite them
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_cluster(mapa(saddr(&c->accempty), 0));
+        }
+        if (kw >= p.c1) continue;
+        if (t == 1) {
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+        const float f = t ? p.scale : 1.f;
+#pragma unroll
+        for (int gq = 0; gq < 2; ++gq) {
+          const uint32_t buf = stg + (uint32_t)gq * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            sts128(buf + ((uint32_t)(k ^ (lane & 7)) << 4), __float_as_uint(__uint_as_float(ra[gq][4 * k]) * f),
+                   __float_as_uint(__uint_as_float(ra[gq][4 * k + 1]) * f),
+                   __float_as_uint(__uint_as_float(ra[gq][4 * k + 2]) * f),
+                   __float_as_uint(__uint_as_float(ra[gq][4 * k + 3]) * f));
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int gq = 0; gq < 2; ++gq)
+            tma_reduce_add_3d(t ? &tmdK : &tmdV, stg + (uint32_t)gq * 4096u, 64 * h + 32 * gq, kw, z);
+          bulk_commit();
+        }
+      }
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->sfree);
+    }
+    if (!ok) fail_f(c, p.status);
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  teardown_f(c, warp);
+}
+
+// ===================================================================== k_attn_q (dQ)
+
+struct QP {
+  int H, T, c0, c1, n_qp, n_units;
+  float scale;
+  const float* lse;
+  const float* D;
+  __nv_bfloat16* dQ;  // [H, T, 128]
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
+// Unit u: head z, queries [c0 + 256 qp, +256) of the chunk, key blocks 0 .. nj-1 (128
+// keys each) up to the unit's last query.  Later query pairs (more keys) first.
+__device__ __forceinline__ void q_unit(const QP& p, int u, int& z, int& qp, int& nj) {
+  const int i = u / p.H;
+  z = u - i * p.H;
+  qp = p.n_qp - 1 - i;
+  const int qend = min(p.c0 + 256 * qp + 256, p.c1);
+  nj = (qend + 127) / 128;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    k_attn_q(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+             const __grid_constant__ CUtensorMap tmKa, const __grid_constant__ CUtensorMap tmVa,
+             const __grid_constant__ CUtensorMap tmKb, const QP p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  CtrlF* c = reinterpret_cast<CtrlF*>(base + Q_CTRL);
+  const uint32_t sb = saddr(base);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ctarank();
+  prologue_f(c, warp);
+  const uint32_t tmem = c->tmem_base;
+  const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // the unit's Q and dO, then ring X: K and V of each key block (this CTA's 64 keys)
+      prefetch_map(&tmQ);
+      prefetch_map(&tmO);
+      prefetch_map(&tmKa);
+      prefetch_map(&tmVa);
+      int sa = 0;
+      uint32_t pha = 0, phr = 0, iss = 0, lph_a[2] = {0, 0}, lph_r = 0;
+      bool ok = true;
+      for (int u = pid; u < p.n_units && ok; u += npairs) {
+        int z, qp, nj;
+        q_unit(p, u, z, qp, nj);
+        if (!wait_bounded(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        const uint32_t fr = mapa(saddr(&c->rfull), 0);
+        if (rank == 0) mbar_expect_tx(&c->rfull, 4u * 32768u);
+        const int qrow = p.c0 + 256 * qp + 128 * (int)rank;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          tma_load_3d_pair(sb + Q_Q + hb * 16384, &tmQ, fr, 64 * hb, qrow, z);
+          tma_load_3d_pair(sb + Q_DO + hb * 16384, &tmO, fr, 64 * hb, qrow, z);
+        }
+        iss |= 4u;
+        lph_r = phr;
+        phr ^= 1u;
+        for (int j = 0; j < nj; ++j) {
+          if (!wait_bounded(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t fa = mapa(saddr(&c->afull[sa]), 0);
+          if (rank == 0) mbar_expect_tx(&c->afull[sa], 2u * Q_X_STAGE);
+          const uint32_t st = sb + Q_X + sa * Q_X_STAGE;
+          const int krow = 128 * j + 64 * (int)rank;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            tma_load_3d_pair(st + hb * 8192, &tmKa, fa, 64 * hb, krow, z);
+            tma_load_3d_pair(st + 16384 + hb * 8192, &tmVa, fa, 64 * hb, krow, z);
+          }
+          iss |= 1u << sa;
+          lph_a[sa] = pha;
+          if (++sa == 2) { sa = 0; pha ^= 1u; }
+        }
+      }
+      if (!ok) {
+        fail_f(c, p.status);
+        if (rank == 0) {
+          if (iss & 4u) wait_bounded(&c->rfull, lph_r, nullptr, 200000000ull);
+          for (int s = 0; s < 2; ++s)
+            if (iss & (1u << s)) wait_bounded(&c->afull[s], lph_a[s], nullptr, 200000000ull);
+        }
+      }
+    } else if (lane == 16) {
+      // ring Y: K of each key block, 128 keys x this CTA's half of hd (B of dQ += dS K)
+      prefetch_map(&tmKb);
+      int sy = 0;
+      uint32_t phy = 0, iss = 0, lph[2] = {0, 0};
+      bool ok = true;
+      for (int u = pid; u < p.n_units && ok; u += npairs) {
+        int z, qp, nj;
+        q_unit(p, u, z, qp, nj);
+        for (int j = 0; j < nj; ++j) {
+          if (!wait_bounded(&c->bempty[sy], phy ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          const uint32_t fb = mapa(saddr(&c->bfull[sy]), 0);
+          if (rank == 0) mbar_expect_tx(&c->bfull[sy], 2u * Q_Y_STAGE);
+          tma_load_3d_pair(sb + Q_Y + sy * Q_Y_STAGE, &tmKb, fb, 64 * (int)rank, 128 * j, z);
+          iss |= 1u << sy;
+          lph[sy] = phy;
+          if (++sy == 2) { sy = 0; phy ^= 1u; }
+        }
+      }
+      if (!ok) {
+        fail_f(c, p.status);
+        if (rank == 0)
+          for (int s = 0; s < 2; ++s)
+            if (iss & (1u << s)) wait_bounded(&c->bfull[s], lph[s], nullptr, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      int sa = 0, sy = 0, lu = 0;
+      uint32_t pha = 0, phy = 0, phr = 0, tempty_seen = 0, oready_seen = 0, acc_seen = 0, g = 0;
+      bool ok = true;
+      // dQ += dS K for global key block gg (the first of its unit overwrites)
+      auto accumulate = [&](uint32_t gg, bool first) -> bool {
+        if (!wait_n(&c->oready, oready_seen, gg + 1, c, p.limit_ns)) return false;
+        if (!wait_bounded(&c->bfull[sy], phy, &c->abort, p.limit_ns)) return false;
+        if (first && !wait_n(&c->accempty, acc_seen, (uint32_t)lu, c, p.limit_ns)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma2_bf16(tmem + 256, sw128_desc(sb + Q_DS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                    sw128_desc(sb + Q_Y + sy * Q_Y_STAGE + k * 2048, 16384, 1024), IDESC_KM,
+                    (!first || k) ? 1u : 0u);
+        commit2_mc(&c->bempty[sy], 3);
+        commit2_mc(&c->ofree, 3);
+        if (++sy == 2) { sy = 0; phy ^= 1u; }
+        return true;
+      };
+      for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
+        int z, qp, nj;
+        q_unit(p, u, z, qp, nj);
+        if (!wait_bounded(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
+        phr ^= 1u;
+        tc_fence_after();
+        for (int n = 0; n < nj; ++n, ++g) {
+          if (!wait_n(&c->tempty, tempty_seen, g, c, p.limit_ns)) { ok = false; break; }
+          if (!wait_bounded(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = sb + Q_X + sa * Q_X_STAGE;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma2_bf16(tmem, sw128_desc(sb + Q_Q + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                      sw128_desc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma2_bf16(tmem + 128, sw128_desc(sb + Q_DO + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                      sw128_desc(st + 16384 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+          commit2_mc(&c->aempty[sa], 3);
+          commit2_mc(&c->tfull, 3);
+          if (n == nj - 1) commit2_mc(&c->rempty, 3);
+          if (++sa == 2) { sa = 0; pha ^= 1u; }
+          if (n >= 1 && !accumulate(g - 1, n == 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!accumulate(g - 1, nj == 1)) { ok = false; break; }
+      }
+      if (!ok) fail_f(c, p.status);
+      commit2_mc(&c->mdone, 1);
+      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int lrow = q * 32 + lane;
+    const uint32_t trow = (uint32_t)(q * 32) << 16;
+    const float sl2 = p.scale * L2E;
+    uint32_t tfull_seen = 0, ofree_seen = 0, g = 0;
+    bool ok = true;
+    for (int u = pid; u < p.n_units && ok; u += npairs) {
+      int z, qp, nj;
+      q_unit(p, u, z, qp, nj);
+      const int qw = p.c0 + 256 * qp + 128 * (int)rank + 32 * q;   // this warp's first query
+      const int qr = qw + lane;                                     // this thread's query
+      const bool vrow = qr < p.c1;
+      const int64_t ro = (int64_t)z * p.T + qr;
+      const float lz = vrow ? p.lse[ro] * L2E : 0.f;
+      const float Dq = vrow ? p.D[ro] : 0.f;
+      for (int j = 0; j < nj; ++j, ++g) {
+        if (!warp_wait_n(&c->tfull, tfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dw[32];   // bf16 pairs of dS over this thread's 64 keys
+#pragma unroll
+        for (int gk = 0; gk < 2; ++gk) {
+          uint32_t rs[32], rd[32];
+          tmem_ld32(tmem + trow + (uint32_t)(64 * h + 32 * gk), rs);
+          tmem_ld32(tmem + trow + (uint32_t)(128 + 64 * h + 32 * gk), rd);
+          tmem_ld_wait();
+          if (gk == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_cluster(mapa(saddr(&c->tempty), 0));
+          }
+          const int kg = 128 * j + 64 * h + 32 * gk;   // first key of the group
+          const bool none = kg > qw + 31 || qw >= p.c1;
+          const bool all = kg + 31 <= qw && qw + 31 < p.c1;
+          if (none) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dw[16 * gk + i] = 0u;
+            continue;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float sv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int jj = 2 * i + e;
+              float pe = ex2(fmaf(__uint_as_float(rs[jj]), sl2, -lz));
+              if (!all && (kg + jj > qr || !vrow)) pe = 0.f;
+              sv[e] = pe * (__uint_as_float(rd[jj]) - Dq);
+            }
+            dw[16 * gk + i] = pack_bf16(sv[0], sv[1]);
+          }
+        }
+        if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
+        store_row128(sb + Q_DS + h * 16384, lrow, dw);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) arrive_cluster(mapa(saddr(&c->oready), 0));
+      }
+      if (!ok) break;
+      // dQ of the unit's queries: s * accumulator, bf16, this thread's row and 64 of hd
+      if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r[2][32];
+      tmem_ld32(tmem + trow + (uint32_t)(256 + 64 * h), r[0]);
+      tmem_ld32(tmem + trow + (uint32_t)(256 + 64 * h + 32), r[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_cluster(mapa(saddr(&c->accempty), 0));
+      if (vrow) {
+        uint4* o = reinterpret_cast<uint4*>(p.dQ + ro * 128 + 64 * h);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* v = &r[k >> 2][(k & 3) * 8];
+          o[k] = make_uint4(pack_bf16(__uint_as_float(v[0]) * p.scale, __uint_as_float(v[1]) * p.scale),
+                            pack_bf16(__uint_as_float(v[2]) * p.scale, __uint_as_float(v[3]) * p.scale),
+                            pack_bf16(__uint_as_float(v[4]) * p.scale, __uint_as_float(v[5]) * p.scale),
+                            pack_bf16(__uint_as_float(v[6]) * p.scale, __uint_as_float(v[7]) * p.scale));
+        }
+      }
+    }
+    if (!ok) fail_f(c, p.status);
+  }
+  teardown_f(c, warp);
+}
+
+}  // namespace fa
+}  // namespace tc
+
+// ========================================================================== host side
+
+namespace {
+
+// 3-D bf16 map over [H, T, 128] (dims hd, T, H): boxes of 64 x rows x 1, 128-byte swizzle,
+// zero fill past T in each head.
+bool map3_bf16(CUtensorMap* m, const void* ptr, int64_t T, int64_t H, uint32_t rows) {
+  auto enc = tc::encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)T, (cuuint64_t)H};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)T * 128 * 2};
+  cuuint32_t box[3] = {64, rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D fp32 map over [H, T, 128] for the dK / dV reduce-adds: 32 x 32 x 1 boxes.
+bool map3_f32(CUtensorMap* m, void* ptr, int64_t T, int64_t H) {
+  auto enc = tc::encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)T, (cuuint64_t)H};
+  cuuint64_t strides[2] = {128 * 4, (cuuint64_t)T * 128 * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool fused_attrs() {
+  static int done = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done == 0) {
+    const bool ok = cudaFuncSetAttribute(tc::fa::k_attn_kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::fa::SMEM_KV) == cudaSuccess &&
+                    cudaFuncSetAttribute(tc::fa::k_attn_q, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::fa::SMEM_Q) == cudaSuccess;
+    done = ok ? 1 : -1;
+  }
+  return done == 1;
+}
+
+}  // namespace
+
+bool AttnFusedPlan::init(const void* Q, const void* K, const void* V, const void* dO, float* dK_, float* dV_,
+                         int64_t T_, int64_t H_) {
+  T = T_;
+  H = H_;
+  return map3_bf16(&K128, K, T, H, 128) && map3_bf16(&V128, V, T, H, 128) && map3_bf16(&Q64, Q, T, H, 64) &&
+         map3_bf16(&O64, dO, T, H, 64) && map3_bf16(&Q128, Q, T, H, 128) && map3_bf16(&O128, dO, T, H, 128) &&
+         map3_bf16(&K64, K, T, H, 64) && map3_bf16(&V64, V, T, H, 64) && map3_f32(&dK, dK_, T, H) &&
+         map3_f32(&dV, dV_, T, H);
+}
+
+cudaError_t attn_fused_kv(const AttnFusedPlan& plan, int64_t c0, int64_t c1, float scale, const float* lse,
+                          const float* D, int32_t* status, cudaStream_t s) {
+  using namespace tc;
+  using namespace tc::fa;
+  if (!fused_attrs()) return cudaErrorInvalidConfiguration;
+  KvP p;
+  p.H = (int)plan.H; p.T = (int)plan.T; p.c0 = (int)c0; p.c1 = (int)c1;
+  p.nb = (int)((c1 - c0 + 127) / 128);
+  p.n_units = (int)((c1 + 255) / 256) * p.H;
+  p.scale = scale; p.lse = lse; p.D = D; p.status = status; p.limit_ns = wait_limit_ns();
+  int pairs = max_pairs((const void*)k_attn_kv, SMEM_KV, KV_THREADS);
+  if (pairs > p.n_units) pairs = p.n_units;
+  k_attn_kv<<<2 * pairs, KV_THREADS, SMEM_KV, s>>>(plan.K128, plan.V128, plan.Q64, plan.O64, plan.Q128, plan.O128,
+                                                   plan.dK, plan.dV, p);
+  return cudaGetLastError();
+}
+
+cudaError_t attn_fused_q(const AttnFusedPlan& plan, int64_t c0, int64_t c1, float scale, const float* lse,
+                         const float* D, void* dQ, int32_t* status, cudaStream_t s) {
+  using namespace tc;
+  using namespace tc::fa;
+  if (!fused_attrs()) return cudaErrorInvalidConfiguration;
+  QP p;
+  p.H = (int)plan.H; p.T = (int)plan.T; p.c0 = (int)c0; p.c1 = (int)c1;
+  p.n_qp = (int)((c1 - c0 + 255) / 256);
+  p.n_units = p.n_qp * p.H;
+  p.scale = scale; p.lse = lse; p.D = D; p.dQ = static_cast<__nv_bfloat16*>(dQ);
+  p.status = status; p.limit_ns = wait_limit_ns();
+  int pairs = max_pairs((const void*)k_attn_q, SMEM_Q);
+  if (pairs > p.n_units) pairs = p.n_units;
+  k_attn_q<<<2 * pairs, NUM_THREADS, SMEM_Q, s>>>(plan.Q128, plan.O128, plan.K64, plan.V64, plan.K128, p);
+  return cudaGetLastError();
+}
+
+}  // namespace sbp

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/sbp.h"
@@ -101,6 +102,21 @@ struct TcAttnArgs {
   int32_t* status;
 };
 cudaError_t tc_attn(const TcAttnArgs& a, bool ds, cudaStream_t s);
+
+// Fused causal-attention backward at head dimension 128, sbp_attn_fused.cu: per chunk
+// of queries [c0, c1), k_attn_kv adds dV and s dK of keys [0, c1) into the fp32 outputs
+// and k_attn_q writes dQ of the chunk's rows (bf16); P and dS never leave the chip.
+// The tensor maps are built once per call (init) and serve every chunk.
+struct AttnFusedPlan {
+  int64_t T = 0, H = 0;
+  CUtensorMap K128, V128, Q64, O64, Q128, O128, K64, V64, dK, dV;
+  bool init(const void* Q, const void* K, const void* V, const void* dO, float* dK, float* dV, int64_t T,
+            int64_t H);
+};
+cudaError_t attn_fused_kv(const AttnFusedPlan& plan, int64_t c0, int64_t c1, float scale, const float* lse,
+                          const float* D, int32_t* status, cudaStream_t s);
+cudaError_t attn_fused_q(const AttnFusedPlan& plan, int64_t c0, int64_t c1, float scale, const float* lse,
+                         const float* D, void* dQ, int32_t* status, cudaStream_t s);
 
 // SIMT fp32 kernels (fp32 operands), sbp_simt.cu
 cudaError_t simt_forward(const float* H, const float* W, int64_t d, int64_t V, int64_t r0, int rows,

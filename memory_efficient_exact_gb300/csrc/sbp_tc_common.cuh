@@ -365,7 +365,7 @@ inline uint64_t wait_limit_ns() {
 
 // Clusters of two (SM pairs) of `kernel` that can be resident at once, cached per
 // device and kernel.
-inline int max_pairs(const void* kernel, size_t smem_bytes) {
+inline int max_pairs(const void* kernel, size_t smem_bytes, int threads = NUM_THREADS) {
   struct Entry { const void* k; int dev; int n; };
   static Entry cache[32] = {};
   static std::mutex mu;
@@ -376,7 +376,7 @@ inline int max_pairs(const void* kernel, size_t smem_bytes) {
     if (e.k == kernel && e.dev == dev && e.n > 0) return e.n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 76, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;

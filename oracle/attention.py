@@ -77,3 +77,30 @@ def backward_chunked(Q, K, V, O, dO, lse, scale: float, chunk: int) -> dict:
             dK[h, :c1] += scale * (dS.T @ Q[h, c0:c1])
             dV[h, :c1] += P.T @ dO[h, c0:c1]
     return dict(dQ=dQ, dK=dK, dV=dV)
+
+
+def rows_dQ(Q, K, V, O, dO, lse, scale: float, h: int, rows) -> np.ndarray:
+    """dQ[h, t] for the listed query rows t, each from its own score row over keys
+    0..t (the causal row of the backward above; cost O(T hd) per row)."""
+    Q, K, V, O, dO, lse = (_f64(a) for a in (Q, K, V, O, dO, lse))
+    out = np.empty((len(rows), Q.shape[2]))
+    for i, t in enumerate(rows):
+        p = np.exp(scale * (K[h, :t + 1] @ Q[h, t]) - lse[h, t])
+        ds = p * (V[h, :t + 1] @ dO[h, t] - dO[h, t] @ O[h, t])
+        out[i] = scale * (ds @ K[h, :t + 1])
+    return out
+
+
+def keys_dKdV(Q, K, V, O, dO, lse, scale: float, h: int, keys):
+    """dK[h, k] and dV[h, k] for the listed keys k, each from its own score column over
+    queries k..T-1 (the causal column of the backward above; cost O(T hd) per key)."""
+    Q, K, V, O, dO, lse = (_f64(a) for a in (Q, K, V, O, dO, lse))
+    hd = Q.shape[2]
+    dK, dV = np.empty((len(keys), hd)), np.empty((len(keys), hd))
+    for i, k in enumerate(keys):
+        p = np.exp(scale * (Q[h, k:] @ K[h, k]) - lse[h, k:])
+        D = (dO[h, k:] * O[h, k:]).sum(axis=1)
+        ds = p * (dO[h, k:] @ V[h, k] - D)
+        dK[i] = scale * (ds @ Q[h, k:])
+        dV[i] = p @ dO[h, k:]
+    return dK, dV

@@ -42,8 +42,14 @@ def dev(x, dt=torch.bfloat16):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dt).contiguous()
 
 
+# hd = 128 runs the fused kernels (P and dS on chip), other widths the chunk-buffer path.
+# The hd = 128 cases cover one token, chunks of one token, chunks that are not multiples
+# of the 128-query block, a chunk equal to T, several 256-key units per head, and more
+# units than SM pairs (H = 48), so that every barrier crosses unit boundaries.
 @pytest.mark.parametrize("H,T,hd,chunk", [(2, 300, 64, 128), (4, 640, 128, 256), (3, 513, 128, 200),
-                                          (1, 1024, 64, 1024), (2, 96, 128, 40)])
+                                          (1, 1024, 64, 1024), (2, 96, 128, 40), (1, 1, 128, 1),
+                                          (2, 5, 128, 3), (2, 67, 128, 1), (1, 700, 128, 700),
+                                          (2, 1100, 128, 384), (48, 1024, 128, 512), (1, 260, 192, 100)])
 def test_attention_backward_parity(sbp, H, T, hd, chunk):
     Q, K, V, O, dO, lse, scale = make(H, T, hd, seed=H * 1000 + T)
     out = sbp.attn_causal_backward(dev(Q), dev(K), dev(V), dev(O), dev(dO), dev(lse, torch.float32), scale, chunk)
@@ -56,8 +62,9 @@ def test_attention_backward_parity(sbp, H, T, hd, chunk):
     assert max(e.values()) <= 2e-2, e
 
 
-def test_attention_accumulate_and_determinism(sbp):
-    H, T, hd, chunk = 2, 300, 64, 128
+@pytest.mark.parametrize("hd", [64, 128])
+def test_attention_accumulate_and_determinism(sbp, hd):
+    H, T, chunk = 2, 300, 128
     Q, K, V, O, dO, lse, scale = make(H, T, hd, seed=7)
     args = [dev(Q), dev(K), dev(V), dev(O), dev(dO), dev(lse, torch.float32), scale, chunk]
     a = sbp.attn_causal_backward(*args)
@@ -69,3 +76,46 @@ def test_attention_accumulate_and_determinism(sbp):
     torch.cuda.synchronize()
     for acc, ref in ((dK, a["dK"]), (dV, a["dV"])):
         assert torch.allclose(acc, 2 * ref, rtol=1e-5, atol=1e-6 * ref.abs().max().item())
+
+
+def test_attention_fullsize_sampled(sbp):
+    """The benchmark's workload and launch configuration (H=32, T=8192, hd=128, chunk
+    1024): dQ on sampled query rows and dK, dV on sampled keys of two heads against the
+    oracle's row and column forms (chunk starts and ends, the first and last token,
+    random picks).  The two heads' O and lse come from the oracle's forward; the other
+    heads' from a plain fp32 torch forward (they only have to be valid inputs)."""
+    H, T, hd, chunk = 32, 8192, 128, 1024
+    g = np.random.default_rng(81920)
+    Q, K, V, dO = (I.round_bf16(g.standard_normal((H, T, hd), dtype=np.float32)) for _ in range(4))
+    scale = 1.0 / np.sqrt(hd)
+    tq, tk, tv, tdo = dev(Q), dev(K), dev(V), dev(dO)
+    O = torch.empty_like(tq)
+    lse = torch.empty((H, T), dtype=torch.float32, device="cuda")
+    mask = torch.ones((T, T), dtype=torch.bool, device="cuda").triu(1)
+    for h in range(H):
+        S = (tq[h].float() @ tk[h].float().T) * scale
+        S.masked_fill_(mask, float("-inf"))
+        lse[h] = torch.logsumexp(S, dim=1)
+        O[h] = (torch.exp(S - lse[h][:, None]) @ tv[h].float()).to(torch.bfloat16)
+    del S, mask
+    heads = (0, H - 1)
+    On = O.float().cpu().numpy()
+    lsen = lse.cpu().numpy()
+    for h in heads:
+        f = A.forward(Q[h:h + 1], K[h:h + 1], V[h:h + 1], scale)
+        On[h] = I.round_bf16(f["O"][0].astype(np.float32))
+        lsen[h] = f["lse"][0].astype(np.float32)
+        O[h] = dev(On[h])
+        lse[h] = torch.from_numpy(lsen[h]).cuda()
+    out = sbp.attn_causal_backward(tq, tk, tv, O, tdo, lse, scale, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    edges = [0, 1, 127, 128, 255, 256, 1023, 1024, 1025, 4095, 4096, 7167, 7168, 8190, 8191]
+    rows = sorted(set(edges) | set(g.integers(0, T, 20).tolist()))
+    keys = sorted(set(edges) | set(g.integers(0, T, 20).tolist()))
+    dQ, dK, dV = (out[k][list(heads)].float().cpu().numpy() for k in ("dQ", "dK", "dV"))
+    for i, h in enumerate(heads):
+        rq = A.rows_dQ(Q, K, V, On, dO, lsen, scale, h, rows)
+        rk, rv = A.keys_dKdV(Q, K, V, On, dO, lsen, scale, h, keys)
+        e = {"dQ": rel_fro(dQ[i][rows], rq), "dK": rel_fro(dK[i][keys], rk), "dV": rel_fro(dV[i][keys], rv)}
+        assert max(e.values()) <= 2e-2, (h, e)

@@ -85,3 +85,19 @@ def test_planted_missing_causal_mask_is_caught(monkeypatch):
     monkeypatch.setattr(np, "triu", real)
     ref = A.backward(Q, K, V, f["O"], dO, f["lse"], 0.5)
     assert np.abs(b["dV"] - ref["dV"]).max() > 1e-3
+
+
+def test_row_and_column_functions_match_the_full_backward():
+    # the sampled-row forms the full-size GPU test uses, against the pinned full backward
+    g = np.random.default_rng(11)
+    H, T, hd, s = 2, 23, 6, 0.45
+    Q, K, V, dO = (g.standard_normal((H, T, hd)) for _ in range(4))
+    f = A.forward(Q, K, V, s)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+    rows, keys = [0, 1, 11, 22], [0, 5, 21, 22]
+    for h in range(H):
+        np.testing.assert_allclose(A.rows_dQ(Q, K, V, f["O"], dO, f["lse"], s, h, rows), b["dQ"][h, rows],
+                                   rtol=1e-12, atol=1e-13)
+        dK, dV = A.keys_dKdV(Q, K, V, f["O"], dO, f["lse"], s, h, keys)
+        np.testing.assert_allclose(dK, b["dK"][h, keys], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(dV, b["dV"][h, keys], rtol=1e-12, atol=1e-13)
