@@ -29,7 +29,16 @@ namespace sbp {
 namespace tc {
 namespace fa {
 
-constexpr int KV_THREADS = NUM_THREADS + 32;  // + one warp that stages lse and D per block
+// Warps: 0 TMA producers, 1 MMA issuer, 2-17 epilogue (lane quadrant warp % 4, 32 of the
+// 128 columns each: sixteen warps, so that the exp / scale / pack chains of four warps
+// per scheduler hide each other's latency), then (k_attn_kv) one warp that stages lse
+// and D per block, and one forwarder warp.  The epilogue warps arrive on CTA-local
+// barriers; the forwarder turns each completed local phase into one arrival at the
+// leader, which keeps the remote arrival's latency off the epilogue's critical path.
+constexpr int FA_EPI = 16;
+constexpr int KV_LD_WARP = 2 + FA_EPI, KV_FWD_WARP = KV_LD_WARP + 1, Q_FWD_WARP = 2 + FA_EPI;
+constexpr int KV_THREADS = 32 * (KV_FWD_WARP + 1);
+constexpr int Q_THREADS = 32 * (Q_FWD_WARP + 1);
 constexpr uint32_t IDESC_KK = idesc_bf16(256, 128, false, false);  // A, B K-major
 constexpr uint32_t IDESC_KM = idesc_bf16(256, 128, false, true);   // A K-major, B MN-major
 
@@ -59,8 +68,9 @@ struct CtrlF {
   uint64_t afull[2], aempty[2];  // ring of the S / dP B operands
   uint64_t bfull[2], bempty[2];  // ring of the B operands of the accumulating GEMMs
   uint64_t rfull, rempty;        // the unit's resident A operands
-  uint64_t tfull, tempty;        // S and dP accumulators
-  uint64_t oready, ofree;        // P^T, dS^T (or dS) in shared memory
+  uint64_t tfull, tempty;        // S and dP accumulators (tempty: leader, one arrival per CTA)
+  uint64_t oready, ofree;        // P^T, dS^T (or dS) in shared memory (oready: leader, one per CTA)
+  uint64_t tempty_l, oready_l;   // the CTA's 8 epilogue warps, forwarded to tempty / oready
   uint64_t accempty;             // the unit's accumulators have been read out
   uint64_t lfull, lempty;        // lse / D of the block (k_attn_kv)
   uint64_t sfree;                // the dV / dK staging has left shared memory (k_attn_kv)
@@ -84,13 +94,15 @@ __device__ __forceinline__ void prologue_f(CtrlF* c, int warp) {
     mbar_init(&c->rfull, 1);
     mbar_init(&c->rempty, 1);
     mbar_init(&c->tfull, 1);
-    mbar_init(&c->tempty, 2 * NUM_EPI_WARPS);
-    mbar_init(&c->oready, 2 * NUM_EPI_WARPS);
+    mbar_init(&c->tempty, 2);
+    mbar_init(&c->oready, 2);
+    mbar_init(&c->tempty_l, FA_EPI);
+    mbar_init(&c->oready_l, FA_EPI);
     mbar_init(&c->ofree, 1);
-    mbar_init(&c->accempty, 2 * NUM_EPI_WARPS);
+    mbar_init(&c->accempty, 2 * FA_EPI);
     mbar_init(&c->lfull, 1);
-    mbar_init(&c->lempty, NUM_EPI_WARPS);
-    mbar_init(&c->sfree, NUM_EPI_WARPS);
+    mbar_init(&c->lempty, FA_EPI);
+    mbar_init(&c->sfree, FA_EPI);
     mbar_init(&c->mdone, 1);
     c->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -141,6 +153,17 @@ __device__ __forceinline__ bool warp_wait_n(uint64_t* b, uint32_t& seen, uint32_
   return true;
 }
 
+// The forwarder: for block g, waits for the CTA's 8 epilogue warps on tempty_l, then on
+// oready_l, and passes each on to the leader's barrier.
+__device__ __forceinline__ bool forward_block(CtrlF* c, uint32_t g, uint32_t& te_seen, uint32_t& or_seen,
+                                              uint64_t limit) {
+  if (!wait_n(&c->tempty_l, te_seen, g + 1, c, limit)) return false;
+  arrive_remote(mapa(saddr(&c->tempty), 0));
+  if (!wait_n(&c->oready_l, or_seen, g + 1, c, limit)) return false;
+  arrive_remote(mapa(saddr(&c->oready), 0));
+  return true;
+}
+
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar_cluster, int x,
                                                  int y, int z) {
   asm volatile(
@@ -156,18 +179,31 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
                : "memory");
 }
 
+// 2^a and 2^b (fp32 special-function unit; measured faster here than the packed
+// half-precision form, whose conversions cost more than the halved exp count saves).
+__device__ __forceinline__ float2 exp2_pair(float a, float b) { return make_float2(ex2(a), ex2(b)); }
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Row `row` (128 B = 64 bf16) of a 128-byte-swizzled K-major tile: 16-byte chunk k at
-// chunk k ^ (row % 8), the layout TMA writes and tcgen05.mma reads.
-__device__ __forceinline__ void store_row128(uint32_t tile, int row, const uint32_t (&w)[32]) {
+// Half `half` (64 B = 32 bf16) of row `row` of a 128-byte-swizzled K-major tile: 16-byte
+// chunk k of the row sits at chunk k ^ (row % 8), the layout TMA writes and tcgen05.mma
+// reads.
+__device__ __forceinline__ void store_half_row(uint32_t tile, int row, int half, const uint32_t (&w)[16]) {
   const uint32_t r = tile + (uint32_t)row * 128u;
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    sts128(r + ((uint32_t)(k ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  for (int k = 0; k < 4; ++k)
+    sts128(r + ((uint32_t)((4 * half + k) ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 // ================================================================ k_attn_kv (dK, dV)
@@ -341,9 +377,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
     }
     __syncwarp();
-  } else if (warp == NUM_EPI_WARPS + 2) {
+  } else if (warp == KV_FWD_WARP) {
+    if (lane == 0) {
+      uint32_t te_seen = 0, or_seen = 0, g = 0;
+      bool ok = true;
+      for (int u = pid; u < p.n_units && ok; u += npairs) {
+        int z, kp, b0;
+        kv_unit(p, u, z, kp, b0);
+        for (int b = b0; b < p.nb; ++b, ++g)
+          if (!forward_block(c, g, te_seen, or_seen, p.limit_ns)) { ok = false; break; }
+      }
+      if (!ok) fail_f(c, p.status);
+    }
+    __syncwarp();
+  } else if (warp == KV_LD_WARP) {
     // lse * log2(e) and D of each block's 128 queries into shared memory (one buffer,
-    // refilled once the 8 epilogue warps have read it); loads issued a block ahead
+    // refilled once the epilogue warps have read it); loads issued a block ahead
     float* ld = reinterpret_cast<float*>(base + KV_LD);
     uint32_t lempty_seen = 0, g = 0;
     for (int u = pid; u < p.n_units; u += npairs) {
@@ -375,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       }
     }
   } else {
-    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int q = warp & 3, cg = (warp - 2) >> 2;   // lane quadrant, 32-column group
     const int lrow = q * 32 + lane;
     const uint32_t trow = (uint32_t)(q * 32) << 16;
     const float sl2 = p.scale * L2E;
@@ -392,45 +441,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         if (!warp_wait_n(&c->tfull, tfull_seen, g + 1, c, p.limit_ns) ||
             !warp_wait_n(&c->lfull, lfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
-        uint32_t pw[32], dw[32];   // bf16 pairs of P^T and dS^T over this thread's 64 queries
+        uint32_t pw[16], dw[16];   // bf16 pairs of P^T and dS^T over this thread's 32 queries
 #pragma unroll
-        for (int gq = 0; gq < 2; ++gq) {
-          uint32_t rs[32], rd[32];
-          tmem_ld32(tmem + trow + (uint32_t)(64 * h + 32 * gq), rs);
-          tmem_ld32(tmem + trow + (uint32_t)(128 + 64 * h + 32 * gq), rd);
+        for (int r = 0; r < 2; ++r) {   // two rounds of 16 queries
+          uint32_t rs[16], rd[16];
+          tmem_ld16(tmem + trow + (uint32_t)(32 * cg + 16 * r), rs);
+          tmem_ld16(tmem + trow + (uint32_t)(128 + 32 * cg + 16 * r), rd);
           tmem_ld_wait();
-          if (gq == 1) {   // S^T and dP^T are in registers: the next block's may be formed
+          if (r == 1) {   // S^T and dP^T are in registers: the next block's may be formed
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) arrive_cluster(mapa(saddr(&c->tempty), 0));
+            if (lane == 0) mbar_arrive(&c->tempty_l);
           }
-          const int qg = p.c0 + 128 * b + 64 * h + 32 * gq;   // first query of the group
-          const bool none = qg + 31 < kw || qg >= p.c1;
-          const bool all = qg >= kw + 31 && qg + 31 < p.c1;
+          const int qg = p.c0 + 128 * b + 32 * cg + 16 * r;   // first query of the round
+          const bool none = qg + 15 < kw || qg >= p.c1;
+          const bool all = qg >= kw + 31 && qg + 15 < p.c1;
           if (none) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) pw[16 * gq + j] = dw[16 * gq + j] = 0u;
+            for (int j = 0; j < 8; ++j) pw[8 * r + j] = dw[8 * r + j] = 0u;
             continue;
           }
-          const float4* l4 = reinterpret_cast<const float4*>(ld + 64 * h + 32 * gq);
-          const float4* d4 = reinterpret_cast<const float4*>(ld + 128 + 64 * h + 32 * gq);
+          const float4* l4 = reinterpret_cast<const float4*>(ld + 32 * cg + 16 * r);
+          const float4* d4 = reinterpret_cast<const float4*>(ld + 128 + 32 * cg + 16 * r);
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
+          for (int j4 = 0; j4 < 4; ++j4) {
             const float4 L = l4[j4], Dv = d4[j4];
             const float lz[4] = {L.x, L.y, L.z, L.w}, dz[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
             float pv[4], sv[4];
 #pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const int j = 4 * j4 + e;
+              const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[j]), sl2, -lz[e]),
+                                          fmaf(__uint_as_float(rs[j + 1]), sl2, -lz[e + 1]));
+              pv[e] = pp.x;
+              pv[e + 1] = pp.y;
+            }
+#pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 4 * j4 + e;
-              float pe = ex2(fmaf(__uint_as_float(rs[j]), sl2, -lz[e]));
-              if (!all && (qg + j < key || qg + j >= p.c1)) pe = 0.f;
-              pv[e] = pe;
-              sv[e] = pe * (__uint_as_float(rd[j]) - dz[e]);
+              if (!all && (qg + j < key || qg + j >= p.c1)) pv[e] = 0.f;
+              sv[e] = pv[e] * (__uint_as_float(rd[j]) - dz[e]);
             }
-            pw[16 * gq + 2 * j4] = pack_bf16(pv[0], pv[1]);
-            pw[16 * gq + 2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
-            dw[16 * gq + 2 * j4] = pack_bf16(sv[0], sv[1]);
-            dw[16 * gq + 2 * j4 + 1] = pack_bf16(sv[2], sv[3]);
+            pw[8 * r + 2 * j4] = pack_bf16(pv[0], pv[1]);
+            pw[8 * r + 2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
+            dw[8 * r + 2 * j4] = pack_bf16(sv[0], sv[1]);
+            dw[8 * r + 2 * j4 + 1] = pack_bf16(sv[2], sv[3]);
           }
         }
         __syncwarp();
@@ -439,29 +494,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         // block, also the previous unit's dV / dK staging has left this area
         if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns) ||
             (b == b0 && !warp_wait_n(&c->sfree, sfree_seen, (uint32_t)lu, c, p.limit_ns))) { ok = false; break; }
-        store_row128(sb + KV_PT + h * 16384, lrow, pw);
-        store_row128(sb + KV_DST + h * 16384, lrow, dw);
+        store_half_row(sb + KV_PT + (cg >> 1) * 16384, lrow, cg & 1, pw);
+        store_half_row(sb + KV_DST + (cg >> 1) * 16384, lrow, cg & 1, dw);
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) arrive_cluster(mapa(saddr(&c->oready), 0));
+        if (lane == 0) mbar_arrive(&c->oready_l);
       }
       if (!ok) break;
-      // the unit's dV and dK: out of tensor memory, through this warp's 8 KB of the
+      // the unit's dV and dK: out of tensor memory, through this warp's 4 KB of the
       // P^T / dS^T area, added into the fp32 outputs.  Each output element receives one
       // add per launch; rows past T are clipped by the tensor map, rows in [c1, T) add 0.
       if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t stg = sb + KV_PT + (uint32_t)(warp - 2) * 8192u;
+      const uint32_t stg = sb + KV_PT + (uint32_t)(warp - 2) * 4096u;
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {   // t = 0: dV, t = 1: s dK
-        uint32_t ra[2][32];
-        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 64 * h), ra[0]);
-        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 64 * h + 32), ra[1]);
+        uint32_t ra[32];
+        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 32 * cg), ra);
         tmem_ld_wait();
         if (t == 1) {   // both accumulators are in registers: the next unit may overwrite them
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) arrive_cluster(mapa(saddr(&c->accempty), 0));
+          if (lane == 0) arrive_remote(mapa(saddr(&c->accempty), 0));
         }
         if (kw >= p.c1) continue;
         if (t == 1) {
@@ -469,22 +523,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
           __syncwarp();
         }
         const float f = t ? p.scale : 1.f;
+        const uint32_t buf = stg + (uint32_t)lane * 128u;
 #pragma unroll
-        for (int gq = 0; gq < 2; ++gq) {
-          const uint32_t buf = stg + (uint32_t)gq * 4096u + (uint32_t)lane * 128u;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            sts128(buf + ((uint32_t)(k ^ (lane & 7)) << 4), __float_as_uint(__uint_as_float(ra[gq][4 * k]) * f),
-                   __float_as_uint(__uint_as_float(ra[gq][4 * k + 1]) * f),
-                   __float_as_uint(__uint_as_float(ra[gq][4 * k + 2]) * f),
-                   __float_as_uint(__uint_as_float(ra[gq][4 * k + 3]) * f));
-        }
+        for (int k = 0; k < 8; ++k)
+          sts128(buf + ((uint32_t)(k ^ (lane & 7)) << 4), __float_as_uint(__uint_as_float(ra[4 * k]) * f),
+                 __float_as_uint(__uint_as_float(ra[4 * k + 1]) * f), __float_as_uint(__uint_as_float(ra[4 * k + 2]) * f),
+                 __float_as_uint(__uint_as_float(ra[4 * k + 3]) * f));
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-#pragma unroll
-          for (int gq = 0; gq < 2; ++gq)
-            tma_reduce_add_3d(t ? &tmdK : &tmdV, stg + (uint32_t)gq * 4096u, 64 * h + 32 * gq, kw, z);
+          tma_reduce_add_3d(t ? &tmdK : &tmdV, stg, 32 * cg, kw, z);
           bulk_commit();
         }
       }
@@ -521,7 +569,7 @@ __device__ __forceinline__ void q_unit(const QP& p, int u, int& z, int& qp, int&
   nj = (qend + 127) / 128;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
     k_attn_q(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
              const __grid_constant__ CUtensorMap tmKa, const __grid_constant__ CUtensorMap tmVa,
              const __grid_constant__ CUtensorMap tmKb, const QP p) {
@@ -664,8 +712,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
     }
     __syncwarp();
+  } else if (warp == Q_FWD_WARP) {
+    if (lane == 0) {
+      uint32_t te_seen = 0, or_seen = 0, g = 0;
+      bool ok = true;
+      for (int u = pid; u < p.n_units && ok; u += npairs) {
+        int z, qp, nj;
+        q_unit(p, u, z, qp, nj);
+        for (int j = 0; j < nj; ++j, ++g)
+          if (!forward_block(c, g, te_seen, or_seen, p.limit_ns)) { ok = false; break; }
+      }
+      if (!ok) fail_f(c, p.status);
+    }
+    __syncwarp();
   } else {
-    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int q = warp & 3, cg = (warp - 2) >> 2;   // lane quadrant, 32-column group
     const int lrow = q * 32 + lane;
     const uint32_t trow = (uint32_t)(q * 32) << 16;
     const float sl2 = p.scale * L2E;
@@ -683,61 +744,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < nj; ++j, ++g) {
         if (!warp_wait_n(&c->tfull, tfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
-        uint32_t dw[32];   // bf16 pairs of dS over this thread's 64 keys
+        uint32_t dw[16];   // bf16 pairs of dS over this thread's 32 keys
 #pragma unroll
-        for (int gk = 0; gk < 2; ++gk) {
-          uint32_t rs[32], rd[32];
-          tmem_ld32(tmem + trow + (uint32_t)(64 * h + 32 * gk), rs);
-          tmem_ld32(tmem + trow + (uint32_t)(128 + 64 * h + 32 * gk), rd);
+        for (int r = 0; r < 2; ++r) {   // two rounds of 16 keys
+          uint32_t rs[16], rd[16];
+          tmem_ld16(tmem + trow + (uint32_t)(32 * cg + 16 * r), rs);
+          tmem_ld16(tmem + trow + (uint32_t)(128 + 32 * cg + 16 * r), rd);
           tmem_ld_wait();
-          if (gk == 1) {
+          if (r == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) arrive_cluster(mapa(saddr(&c->tempty), 0));
+            if (lane == 0) mbar_arrive(&c->tempty_l);
           }
-          const int kg = 128 * j + 64 * h + 32 * gk;   // first key of the group
+          const int kg = 128 * j + 32 * cg + 16 * r;   // first key of the round
           const bool none = kg > qw + 31 || qw >= p.c1;
-          const bool all = kg + 31 <= qw && qw + 31 < p.c1;
+          const bool all = kg + 15 <= qw && qw + 31 < p.c1;
           if (none) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dw[16 * gk + i] = 0u;
+            for (int i = 0; i < 8; ++i) dw[8 * r + i] = 0u;
             continue;
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float sv[2];
+          for (int i = 0; i < 8; ++i) {
+            const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[2 * i]), sl2, -lz),
+                                        fmaf(__uint_as_float(rs[2 * i + 1]), sl2, -lz));
+            float pv[2] = {pp.x, pp.y}, sv[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int jj = 2 * i + e;
-              float pe = ex2(fmaf(__uint_as_float(rs[jj]), sl2, -lz));
-              if (!all && (kg + jj > qr || !vrow)) pe = 0.f;
-              sv[e] = pe * (__uint_as_float(rd[jj]) - Dq);
+              if (!all && (kg + jj > qr || !vrow)) pv[e] = 0.f;
+              sv[e] = pv[e] * (__uint_as_float(rd[jj]) - Dq);
             }
-            dw[16 * gk + i] = pack_bf16(sv[0], sv[1]);
+            dw[8 * r + i] = pack_bf16(sv[0], sv[1]);
           }
         }
         if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
-        store_row128(sb + Q_DS + h * 16384, lrow, dw);
+        store_half_row(sb + Q_DS + (cg >> 1) * 16384, lrow, cg & 1, dw);
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) arrive_cluster(mapa(saddr(&c->oready), 0));
+        if (lane == 0) mbar_arrive(&c->oready_l);
       }
       if (!ok) break;
-      // dQ of the unit's queries: s * accumulator, bf16, this thread's row and 64 of hd
+      // dQ of the unit's queries: s * accumulator, bf16, this thread's row and 32 of hd
       if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[2][32];
-      tmem_ld32(tmem + trow + (uint32_t)(256 + 64 * h), r[0]);
-      tmem_ld32(tmem + trow + (uint32_t)(256 + 64 * h + 32), r[1]);
+      uint32_t ra[32];
+      tmem_ld32(tmem + trow + (uint32_t)(256 + 32 * cg), ra);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) arrive_cluster(mapa(saddr(&c->accempty), 0));
+      if (lane == 0) arrive_remote(mapa(saddr(&c->accempty), 0));
       if (vrow) {
-        uint4* o = reinterpret_cast<uint4*>(p.dQ + ro * 128 + 64 * h);
+        uint4* o = reinterpret_cast<uint4*>(p.dQ + ro * 128 + 32 * cg);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t* v = &r[k >> 2][(k & 3) * 8];
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t* v = &ra[8 * k];
           o[k] = make_uint4(pack_bf16(__uint_as_float(v[0]) * p.scale, __uint_as_float(v[1]) * p.scale),
                             pack_bf16(__uint_as_float(v[2]) * p.scale, __uint_as_float(v[3]) * p.scale),
                             pack_bf16(__uint_as_float(v[4]) * p.scale, __uint_as_float(v[5]) * p.scale),
@@ -838,9 +899,9 @@ cudaError_t attn_fused_q(const AttnFusedPlan& plan, int64_t c0, int64_t c1, floa
   p.n_units = p.n_qp * p.H;
   p.scale = scale; p.lse = lse; p.D = D; p.dQ = static_cast<__nv_bfloat16*>(dQ);
   p.status = status; p.limit_ns = wait_limit_ns();
-  int pairs = max_pairs((const void*)k_attn_q, SMEM_Q);
+  int pairs = max_pairs((const void*)k_attn_q, SMEM_Q, Q_THREADS);
   if (pairs > p.n_units) pairs = p.n_units;
-  k_attn_q<<<2 * pairs, NUM_THREADS, SMEM_Q, s>>>(plan.Q128, plan.O128, plan.K64, plan.V64, plan.K128, p);
+  k_attn_q<<<2 * pairs, Q_THREADS, SMEM_Q, s>>>(plan.Q128, plan.O128, plan.K64, plan.V64, plan.K128, p);
   return cudaGetLastError();
 }
 

@@ -161,6 +161,14 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrival on a barrier of the pair with the instruction's default semantics (release at
+// CTA scope), about 500 cycles against about 1300 for the cluster-scope release above
+// (measured on GB300).  Used where the arriving thread has already acquired what it
+// passes on (a forwarder) or where the protected data is tensor memory that has been
+// read out (tcgen05.wait::ld done before the arrival).
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ bool try_cluster(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
