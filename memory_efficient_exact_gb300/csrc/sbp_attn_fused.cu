@@ -61,8 +61,10 @@ constexpr uint32_t Q_X = 65536;       // 2 stages: K then V of the key block, th
 constexpr uint32_t Q_X_STAGE = 32768;
 constexpr uint32_t Q_Y = 131072;      // 2 stages: K of the key block, 128 keys x this CTA's 64 of hd
 constexpr uint32_t Q_Y_STAGE = 16384;
-constexpr uint32_t Q_DS = 163840;     // dS [2 key halves][128 queries][128 B]
-constexpr uint32_t Q_CTRL = 196608;
+constexpr uint32_t Q_CTRL = 163840;
+// Tensor memory of k_attn_q: S [0, 128), dP [128, 256), dQ [256, 384), and two bf16 dS
+// buffers of 64 columns (128 keys) at Q_TDS and Q_TDS + 64: the A operand of dQ += dS K.
+constexpr uint32_t Q_TDS = 384;
 
 struct CtrlF {
   uint64_t afull[2], aempty[2];  // ring of the S / dP B operands
@@ -70,7 +72,8 @@ struct CtrlF {
   uint64_t rfull, rempty;        // the unit's resident A operands
   uint64_t tfull, tempty;        // S and dP accumulators (tempty: leader, one arrival per CTA)
   uint64_t oready, ofree;        // P^T, dS^T (or dS) in shared memory (oready: leader, one per CTA)
-  uint64_t tempty_l, oready_l;   // the CTA's 8 epilogue warps, forwarded to tempty / oready
+  uint64_t tempty_l, oready_l;   // the CTA's epilogue warps, forwarded to tempty / oready
+  uint64_t dsfree[2];            // k_attn_q: the dQ GEMM has read dS buffer 0 / 1 (tensor memory)
   uint64_t accempty;             // the unit's accumulators have been read out
   uint64_t lfull, lempty;        // lse / D of the block (k_attn_kv)
   uint64_t sfree;                // the dV / dK staging has left shared memory (k_attn_kv)
@@ -99,6 +102,8 @@ __device__ __forceinline__ void prologue_f(CtrlF* c, int warp) {
     mbar_init(&c->tempty_l, FA_EPI);
     mbar_init(&c->oready_l, FA_EPI);
     mbar_init(&c->ofree, 1);
+    mbar_init(&c->dsfree[0], 1);
+    mbar_init(&c->dsfree[1], 1);
     mbar_init(&c->accempty, 2 * FA_EPI);
     mbar_init(&c->lfull, 1);
     mbar_init(&c->lempty, FA_EPI);
@@ -197,6 +202,27 @@ __device__ __forceinline__ void store_half_row(uint32_t tile, int row, int half,
   for (int k = 0; k < 4; ++k)
     sts128(r + ((uint32_t)((4 * half + k) ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
+
+// tcgen05.mma with A in tensor memory (each CTA's 128 rows in its lanes, two bf16 of
+// consecutive K per 32-bit column, the lower K in the low half) and B in shared memory.
+__device__ __forceinline__ void mma2_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -442,17 +468,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
             !warp_wait_n(&c->lfull, lfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
         uint32_t pw[16], dw[16];   // bf16 pairs of P^T and dS^T over this thread's 32 queries
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tmem + trow + (uint32_t)(32 * cg), rs);
+        tmem_ld32(tmem + trow + (uint32_t)(128 + 32 * cg), rd);
+        tmem_ld_wait();
+        // S^T and dP^T are in registers: the next block's may be formed
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c->tempty_l);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {   // two rounds of 16 queries
-          uint32_t rs[16], rd[16];
-          tmem_ld16(tmem + trow + (uint32_t)(32 * cg + 16 * r), rs);
-          tmem_ld16(tmem + trow + (uint32_t)(128 + 32 * cg + 16 * r), rd);
-          tmem_ld_wait();
-          if (r == 1) {   // S^T and dP^T are in registers: the next block's may be formed
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&c->tempty_l);
-          }
           const int qg = p.c0 + 128 * b + 32 * cg + 16 * r;   // first query of the round
           const bool none = qg + 15 < kw || qg >= p.c1;
           const bool all = qg >= kw + 31 && qg + 15 < p.c1;
@@ -470,7 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
             float pv[4], sv[4];
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
-              const int j = 4 * j4 + e;
+              const int j = 16 * r + 4 * j4 + e;
               const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[j]), sl2, -lz[e]),
                                           fmaf(__uint_as_float(rs[j + 1]), sl2, -lz[e + 1]));
               pv[e] = pp.x;
@@ -480,7 +505,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
             for (int e = 0; e < 4; ++e) {
               const int j = 4 * j4 + e;
               if (!all && (qg + j < key || qg + j >= p.c1)) pv[e] = 0.f;
-              sv[e] = pv[e] * (__uint_as_float(rd[j]) - dz[e]);
+              sv[e] = pv[e] * (__uint_as_float(rd[16 * r + j]) - dz[e]);
             }
             pw[8 * r + 2 * j4] = pack_bf16(pv[0], pv[1]);
             pw[8 * r + 2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
@@ -671,11 +696,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma2_bf16(tmem + 256, sw128_desc(sb + Q_DS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                    sw128_desc(sb + Q_Y + sy * Q_Y_STAGE + k * 2048, 16384, 1024), IDESC_KM,
-                    (!first || k) ? 1u : 0u);
+          mma2_bf16_ts(tmem + 256, tmem + Q_TDS + 64 * (gg & 1) + 8 * k,
+                       sw128_desc(sb + Q_Y + sy * Q_Y_STAGE + k * 2048, 16384, 1024), IDESC_KM,
+                       (!first || k) ? 1u : 0u);
         commit2_mc(&c->bempty[sy], 3);
-        commit2_mc(&c->ofree, 3);
+        commit2_mc(&c->dsfree[gg & 1], 3);
         if (++sy == 2) { sy = 0; phy ^= 1u; }
         return true;
       };
@@ -730,7 +755,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
     const int lrow = q * 32 + lane;
     const uint32_t trow = (uint32_t)(q * 32) << 16;
     const float sl2 = p.scale * L2E;
-    uint32_t tfull_seen = 0, ofree_seen = 0, g = 0;
+    uint32_t tfull_seen = 0, g = 0;
+    uint32_t ds_seen0 = 0, ds_seen1 = 0, ds_uses0 = 0, ds_uses1 = 0;   // per dS buffer: completions waited, blocks written
     bool ok = true;
     for (int u = pid; u < p.n_units && ok; u += npairs) {
       int z, qp, nj;
@@ -751,7 +777,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
           tmem_ld16(tmem + trow + (uint32_t)(32 * cg + 16 * r), rs);
           tmem_ld16(tmem + trow + (uint32_t)(128 + 32 * cg + 16 * r), rd);
           tmem_ld_wait();
-          if (r == 1) {
+          if (r == 1) {   // S and dP are in registers: the next block's may be formed
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&c->tempty_l);
@@ -778,15 +804,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
             dw[8 * r + i] = pack_bf16(sv[0], sv[1]);
           }
         }
-        if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
-        store_half_row(sb + Q_DS + (cg >> 1) * 16384, lrow, cg & 1, dw);
-        fence_proxy_async();
+        // dS into tensor-memory buffer g % 2 once the dQ GEMM of its previous block has read it
+        const int bf = (int)(g & 1u);
+        if (!(bf ? warp_wait_n(&c->dsfree[1], ds_seen1, ds_uses1, c, p.limit_ns)
+                 : warp_wait_n(&c->dsfree[0], ds_seen0, ds_uses0, c, p.limit_ns))) { ok = false; break; }
+        tmem_st16(tmem + trow + (uint32_t)(Q_TDS + 64 * bf + 16 * cg), dw);
+        tmem_st_wait();
+        if (bf) ++ds_uses1; else ++ds_uses0;
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->oready_l);
       }
       if (!ok) break;
-      // dQ of the unit's queries: s * accumulator, bf16, this thread's row and 32 of hd
-      if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
+      // dQ of the unit's queries: s * accumulator, bf16, this thread's row and 32 of hd (the
+      // commit after the last dQ GEMM covers all earlier ones)
+      if (!(((g - 1u) & 1u) ? warp_wait_n(&c->dsfree[1], ds_seen1, ds_uses1, c, p.limit_ns)
+                            : warp_wait_n(&c->dsfree[0], ds_seen0, ds_uses0, c, p.limit_ns))) { ok = false; break; }
       tc_fence_after();
       uint32_t ra[32];
       tmem_ld32(tmem + trow + (uint32_t)(256 + 32 * cg), ra);
