@@ -193,7 +193,9 @@ int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, cons
  * D_t = dO_t . O_t, dS = P (dO V^T - D),
  *     dQ = s dS K,  dK (+)= s dS^T Q,  dV (+)= P^T dO,
  * computed one chunk of `chunk` queries at a time: chunk [c0, c1) reads keys [0, c1), writes
- * its dQ rows and adds into dK, dV rows [0, c1).  Only one chunk's P and dS exist at a time.
+ * its dQ rows and adds into dK, dV rows [0, c1).  At hd = 128, P and dS stay on chip
+ * (tensor and shared memory) and the workspace holds D only; at other widths one chunk's
+ * P and dS ([H, chunk, T] bf16 each) live in the workspace at a time.
  *   Q, K, V, O, dO [H, T, hd] bf16 (head-major); lse [H, T] fp32, the forward's natural
  *   log-sum-exp of s Q K^T per query row; dQ [H, T, hd] bf16 (overwritten);
  *   dK, dV [H, T, hd] fp32 (overwritten when accumulate = 0, added to when 1).
