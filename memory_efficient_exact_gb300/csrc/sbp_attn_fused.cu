@@ -188,6 +188,13 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
 // half-precision form, whose conversions cost more than the halved exp count saves).
 __device__ __forceinline__ float2 exp2_pair(float a, float b) { return make_float2(ex2(a), ex2(b)); }
 
+// Descriptor d advanced by `bytes` (a multiple of 16 that keeps the start address inside
+// its 14-bit field): one 32-bit add on the low word instead of rebuilding the descriptor
+// for every operand and k-step.
+__device__ __forceinline__ uint64_t dplus(uint64_t d, uint32_t bytes) {
+  return (d & 0xFFFFFFFF00000000ull) | (uint64_t)((uint32_t)d + (bytes >> 4));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -348,6 +355,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       int sa = 0, lu = 0;
       uint32_t pha = 0, phb = 0, phr = 0, tempty_seen = 0, oready_seen = 0, acc_seen = 0, g = 0;
       bool ok = true;
+      const uint64_t dK = sw128_desc(sb + KV_K, 16, 1024), dV = sw128_desc(sb + KV_V, 16, 1024),
+                     dA = sw128_desc(sb + KV_A, 16, 1024), dPT = sw128_desc(sb + KV_PT, 16, 1024),
+                     dDST = sw128_desc(sb + KV_DST, 16, 1024), dBm = sw128_desc(sb + KV_B, 16384, 1024);
       // dV += P^T dO and dK += dS^T Q for global block gg (the first of its unit overwrites)
       auto accumulate = [&](uint32_t gg, bool first) -> bool {
         if (!wait_n(&c->oready, oready_seen, gg + 1, c, p.limit_ns)) return false;
@@ -357,12 +367,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma2_bf16(tmem + 256, sw128_desc(sb + KV_PT + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                    sw128_desc(sb + KV_B + 16384 + k * 2048, 16384, 1024), IDESC_KM, (!first || k) ? 1u : 0u);
+          mma2_bf16(tmem + 256, dplus(dPT, (k >> 2) * 16384 + (k & 3) * 32), dplus(dBm, 16384 + k * 2048), IDESC_KM,
+                    (!first || k) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma2_bf16(tmem + 384, sw128_desc(sb + KV_DST + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                    sw128_desc(sb + KV_B + k * 2048, 16384, 1024), IDESC_KM, (!first || k) ? 1u : 0u);
+          mma2_bf16(tmem + 384, dplus(dDST, (k >> 2) * 16384 + (k & 3) * 32), dplus(dBm, k * 2048), IDESC_KM,
+                    (!first || k) ? 1u : 0u);
         commit2_mc(&c->bempty[0], 3);
         commit2_mc(&c->ofree, 3);
         return true;
@@ -380,15 +390,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
           if (!wait_n(&c->tempty, tempty_seen, g, c, p.limit_ns)) { ok = false; break; }
           if (!wait_bounded(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = sb + KV_A + sa * KV_A_STAGE;
+          const uint64_t dst = dplus(dA, sa * KV_A_STAGE);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma2_bf16(tmem, sw128_desc(sb + KV_K + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                      sw128_desc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+            mma2_bf16(tmem, dplus(dK, (k >> 2) * 16384 + (k & 3) * 32), dplus(dst, (k >> 2) * 8192 + (k & 3) * 32),
+                      IDESC_KK, k ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma2_bf16(tmem + 128, sw128_desc(sb + KV_V + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                      sw128_desc(st + 16384 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+            mma2_bf16(tmem + 128, dplus(dV, (k >> 2) * 16384 + (k & 3) * 32),
+                      dplus(dst, 16384 + (k >> 2) * 8192 + (k & 3) * 32), IDESC_KK, k ? 1u : 0u);
           commit2_mc(&c->aempty[sa], 3);
           commit2_mc(&c->tfull, 3);
           if (n == nbl - 1) commit2_mc(&c->rempty, 3);
@@ -688,6 +698,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
       int sa = 0, sy = 0, lu = 0;
       uint32_t pha = 0, phy = 0, phr = 0, tempty_seen = 0, oready_seen = 0, acc_seen = 0, g = 0;
       bool ok = true;
+      const uint64_t dQd = sw128_desc(sb + Q_Q, 16, 1024), dOd = sw128_desc(sb + Q_DO, 16, 1024),
+                     dX = sw128_desc(sb + Q_X, 16, 1024), dY = sw128_desc(sb + Q_Y, 16384, 1024);
       // dQ += dS K for global key block gg (the first of its unit overwrites)
       auto accumulate = [&](uint32_t gg, bool first) -> bool {
         if (!wait_n(&c->oready, oready_seen, gg + 1, c, p.limit_ns)) return false;
@@ -697,7 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma2_bf16_ts(tmem + 256, tmem + Q_TDS + 64 * (gg & 1) + 8 * k,
-                       sw128_desc(sb + Q_Y + sy * Q_Y_STAGE + k * 2048, 16384, 1024), IDESC_KM,
+                       dplus(dY, sy * Q_Y_STAGE + k * 2048), IDESC_KM,
                        (!first || k) ? 1u : 0u);
         commit2_mc(&c->bempty[sy], 3);
         commit2_mc(&c->dsfree[gg & 1], 3);
@@ -714,15 +726,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
           if (!wait_n(&c->tempty, tempty_seen, g, c, p.limit_ns)) { ok = false; break; }
           if (!wait_bounded(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = sb + Q_X + sa * Q_X_STAGE;
+          const uint64_t dst = dplus(dX, sa * Q_X_STAGE);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma2_bf16(tmem, sw128_desc(sb + Q_Q + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                      sw128_desc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+            mma2_bf16(tmem, dplus(dQd, (k >> 2) * 16384 + (k & 3) * 32), dplus(dst, (k >> 2) * 8192 + (k & 3) * 32),
+                      IDESC_KK, k ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma2_bf16(tmem + 128, sw128_desc(sb + Q_DO + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                      sw128_desc(st + 16384 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), IDESC_KK, k ? 1u : 0u);
+            mma2_bf16(tmem + 128, dplus(dOd, (k >> 2) * 16384 + (k & 3) * 32),
+                      dplus(dst, 16384 + (k >> 2) * 8192 + (k & 3) * 32), IDESC_KK, k ? 1u : 0u);
           commit2_mc(&c->aempty[sa], 3);
           commit2_mc(&c->tfull, 3);
           if (n == nj - 1) commit2_mc(&c->rempty, 3);
