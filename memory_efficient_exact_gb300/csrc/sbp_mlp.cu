@@ -24,7 +24,34 @@ struct MlpP {
   int32_t* status; uint64_t limit_ns;
 };
 
-constexpr size_t SMEM_MLP = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+// The epilogue's bf16 outputs leave through one 32 x 64 staging block (4 KB, 128-byte
+// swizzle) per warp and TMA stores: row-per-thread global stores (32 L2 sectors per
+// request) were measured to starve the operand loads.
+constexpr uint32_t STG_MLP = 32 * 64 * 2;
+constexpr size_t SMEM_MLP = STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_MLP + sizeof(Ctrl) + 1024;
+static_assert(SMEM_MLP <= 232448, "shared memory budget of one CTA");
+
+// Row `lane` of a warp's staging block: 16-byte chunks k0 .. k0+3 from w (chunk k at
+// chunk k ^ (lane % 8)).
+__device__ __forceinline__ void stage4(uint32_t stg, int lane, int k0, const uint32_t* w) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    sts128(stg + lane * 128 + (((k0 + k) ^ (lane & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+// Hands the staging block to TMA (store at column x, row y of `map`) once the previous
+// contents have been read out; the next write must wait for this one to be read.
+__device__ __forceinline__ void stage_store(const CUtensorMap* map, uint32_t stg, int lane, int x, int y) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, stg, x, y);
+    bulk_commit();
+  }
+}
+__device__ __forceinline__ void stage_free(int lane) {
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+}
 constexpr uint32_t IDESC_KK = idesc_bf16(256, 256, false, false);
 constexpr uint32_t IDESC_KM = idesc_bf16(256, 256, false, true);
 
@@ -40,10 +67,12 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 
 template <bool DA>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    k_mlp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const MlpP p) {
+    k_mlp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          const __grid_constant__ CUtensorMap tmAo, const __grid_constant__ CUtensorMap tmGU, const MlpP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  uint8_t* stg_base = base + STAGES * STAGE_BYTES;
+  Ctrl* c = reinterpret_cast<Ctrl*>(stg_base + NUM_EPI_WARPS * STG_MLP);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
   prologue(c, warp);
@@ -133,72 +162,95 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      uint32_t r[4][32];
+      const uint32_t stg = saddr(stg_base + (warp - 2) * STG_MLP);
+      const int yrow = mp * 256 + (int)rank * 128 + q * 32;   // this warp's first row
       __syncwarp();
       if (!DA) {
         // g in accumulator columns [64h, 64h+64), u in [128 + 64h, 128 + 64h + 64)
+        uint32_t r[4][32];
         tmem_ld32(tb + 64 * h, r[0]);
         tmem_ld32(tb + 64 * h + 32, r[1]);
         tmem_ld32(tb + 128 + 64 * h, r[2]);
         tmem_ld32(tb + 128 + 64 * h + 32, r[3]);
-      } else {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) tmem_ld32(tb + 128 * h + g * 32, r[g]);
-      }
-      tmem_ld_wait();
-      release_tmem(c, buf, lane);
-      if (!vrow) continue;
-      __nv_bfloat16* gu = p.GU + (int64_t)row * 2 * p.f;
-      if (!DA) {
-        const int64_t f0 = (int64_t)nb * 128 + 64 * h;
+        tmem_ld_wait();
+        release_tmem(c, buf, lane);
+        const int f0 = nb * 128 + 64 * h;
+        // a = silu(g) u, then g, then u: one 32 x 64 block each (rows past the chunk are
+        // clipped by the tensor maps)
+        stage_free(lane);
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          uint32_t av[16], gv[16], uv[16];
+          uint32_t av[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const float g0 = __uint_as_float(r[g][j]), g1 = __uint_as_float(r[g][j + 1]);
             const float u0 = __uint_as_float(r[2 + g][j]), u1 = __uint_as_float(r[2 + g][j + 1]);
             av[j / 2] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
-            gv[j / 2] = pack_bf16(g0, g1);
-            uv[j / 2] = pack_bf16(u0, u1);
           }
-          uint4* da = reinterpret_cast<uint4*>(p.A + (int64_t)row * p.f + f0 + 32 * g);
-          uint4* dg = reinterpret_cast<uint4*>(gu + f0 + 32 * g);
-          uint4* du = reinterpret_cast<uint4*>(gu + p.f + f0 + 32 * g);
+          stage4(stg, lane, 4 * g, av);
+        }
+        stage_store(&tmAo, stg, lane, f0, yrow);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            da[k] = make_uint4(av[4 * k], av[4 * k + 1], av[4 * k + 2], av[4 * k + 3]);
-            dg[k] = make_uint4(gv[4 * k], gv[4 * k + 1], gv[4 * k + 2], gv[4 * k + 3]);
-            du[k] = make_uint4(uv[4 * k], uv[4 * k + 1], uv[4 * k + 2], uv[4 * k + 3]);
+        for (int t = 0; t < 2; ++t) {   // t = 0: g, t = 1: u
+          stage_free(lane);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint32_t v[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              v[j / 2] = pack_bf16(__uint_as_float(r[2 * t + g][j]), __uint_as_float(r[2 * t + g][j + 1]));
+            stage4(stg, lane, 4 * g, v);
           }
+          stage_store(&tmGU, stg, lane, (t ? p.f : 0) + f0, yrow);
         }
       } else {
-        const int64_t f0 = (int64_t)nb * BN + 128 * h;
+        // this half tile's 128 columns of da in two 64-column blocks; dg and du replace
+        // g and u in place
+        __nv_bfloat16* gu = p.GU + (int64_t)row * 2 * p.f;
+#pragma unroll 1
+        for (int bx = 0; bx < 2; ++bx) {
+          uint32_t r[2][32];
+          tmem_ld32(tb + 128 * h + 64 * bx, r[0]);
+          tmem_ld32(tb + 128 * h + 64 * bx + 32, r[1]);
+          tmem_ld_wait();
+          if (bx == 1) release_tmem(c, buf, lane);
+          const int f0 = nb * BN + 128 * h + 64 * bx;
+          uint32_t duw[2][16];
+          stage_free(lane);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4* pg = reinterpret_cast<uint4*>(gu + f0 + 32 * g);
-          uint4* pu = reinterpret_cast<uint4*>(gu + p.f + f0 + 32 * g);
+          for (int g = 0; g < 2; ++g) {
+            uint32_t dgw[16];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 G4 = pg[k], U4 = pu[k];
-            const uint32_t gw[4] = {G4.x, G4.y, G4.z, G4.w}, uw[4] = {U4.x, U4.y, U4.z, U4.w};
-            uint32_t ow_g[4], ow_u[4];
+            for (int k = 0; k < 4; ++k) {
+              uint4 G4 = make_uint4(0u, 0u, 0u, 0u), U4 = G4;
+              if (vrow) {
+                G4 = reinterpret_cast<const uint4*>(gu + f0 + 32 * g)[k];
+                U4 = reinterpret_cast<const uint4*>(gu + p.f + f0 + 32 * g)[k];
+              }
+              const uint32_t gw[4] = {G4.x, G4.y, G4.z, G4.w}, uw[4] = {U4.x, U4.y, U4.z, U4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 gg = unpack_bf16(gw[e]), uu = unpack_bf16(uw[e]);
-              const float a0 = __uint_as_float(r[g][8 * k + 2 * e]), a1 = __uint_as_float(r[g][8 * k + 2 * e + 1]);
-              const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
-              // dg = da u silu'(g), silu'(g) = s (1 + g (1 - s));  du = da silu(g)
-              ow_g[e] = pack_bf16(a0 * uu.x * s0 * (1.f + gg.x * (1.f - s0)),
-                                  a1 * uu.y * s1 * (1.f + gg.y * (1.f - s1)));
-              ow_u[e] = pack_bf16(a0 * gg.x * s0, a1 * gg.y * s1);
+              for (int e = 0; e < 4; ++e) {
+                const float2 gg = unpack_bf16(gw[e]), uu = unpack_bf16(uw[e]);
+                const float a0 = __uint_as_float(r[g][8 * k + 2 * e]), a1 = __uint_as_float(r[g][8 * k + 2 * e + 1]);
+                const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
+                // dg = da u silu'(g), silu'(g) = s (1 + g (1 - s));  du = da silu(g)
+                dgw[4 * k + e] = pack_bf16(a0 * uu.x * s0 * (1.f + gg.x * (1.f - s0)),
+                                           a1 * uu.y * s1 * (1.f + gg.y * (1.f - s1)));
+                duw[g][4 * k + e] = pack_bf16(a0 * gg.x * s0, a1 * gg.y * s1);
+              }
             }
-            pg[k] = make_uint4(ow_g[0], ow_g[1], ow_g[2], ow_g[3]);
-            pu[k] = make_uint4(ow_u[0], ow_u[1], ow_u[2], ow_u[3]);
+            stage4(stg, lane, 4 * g, dgw);
           }
+          stage_store(&tmGU, stg, lane, f0, yrow);
+          stage_free(lane);
+          stage4(stg, lane, 0, duw[0]);
+          stage4(stg, lane, 4, duw[1]);
+          stage_store(&tmGU, stg, lane, p.f + f0, yrow);
         }
       }
     }
+    if (lane == 0) bulk_wait_all();   // every output block has left shared memory and landed
+    __syncwarp();
   }
   teardown(c, warp);
 }
@@ -231,6 +283,15 @@ cudaError_t tc_mlp(const TcMlpArgs& a, bool da, cudaStream_t s) {
     // B: Wd [d, f] read MN-major: boxes of 64 f-columns x 64 d-rows
     if (!make_map(&mB, a.B, (uint64_t)a.f, (uint64_t)a.d, (uint64_t)a.f, 64, 64)) return cudaErrorInvalidValue;
   }
+  // outputs of the chunk: a [rows, f] and g | u [rows, 2f], bf16, stored in 64 x 32 blocks
+  CUtensorMap mAo, mGU;
+  if (!make_map(&mGU, a.GU, (uint64_t)(2 * a.f), (uint64_t)a.rows, (uint64_t)(2 * a.f), 64, 32))
+    return cudaErrorInvalidValue;
+  if (!da) {
+    if (!make_map(&mAo, a.Aout, (uint64_t)a.f, (uint64_t)a.rows, (uint64_t)a.f, 64, 32)) return cudaErrorInvalidValue;
+  } else {
+    mAo = mGU;
+  }
   MlpP p;
   p.r0 = a.r0; p.rows = a.rows; p.f = a.f;
   p.mt = (a.rows + 255) / 256;
@@ -243,8 +304,8 @@ cudaError_t tc_mlp(const TcMlpArgs& a, bool da, cudaStream_t s) {
   const void* kern = da ? (const void*)k_mlp<true> : (const void*)k_mlp<false>;
   int pairs = max_pairs(kern, SMEM_MLP);
   if (pairs > total) pairs = total;
-  if (da) k_mlp<true><<<2 * pairs, NUM_THREADS, SMEM_MLP, s>>>(mA, mB, p);
-  else k_mlp<false><<<2 * pairs, NUM_THREADS, SMEM_MLP, s>>>(mA, mB, p);
+  if (da) k_mlp<true><<<2 * pairs, NUM_THREADS, SMEM_MLP, s>>>(mA, mB, mAo, mGU, p);
+  else k_mlp<false><<<2 * pairs, NUM_THREADS, SMEM_MLP, s>>>(mA, mB, mAo, mGU, p);
   return cudaGetLastError();
 }
 

@@ -120,15 +120,21 @@ struct BwdP {
 // swizzle) per epilogue warp, handed to the TMA unit for an asynchronous, coalesced
 // reduce-add (or store, first chunk) into dW.
 constexpr uint32_t STG_BYTES = 32 * 32 * 4;
-constexpr size_t SMEM_FWD = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+// k_fwd stages its fp16 exp tile the same way: 32 rows x 64 columns (4 KB, 128-byte
+// swizzle) per epilogue warp at a time, written out by TMA stores.  Row-per-thread global
+// stores (32 L2 sectors per request) were measured to starve the operand loads.
+constexpr size_t SMEM_FWD = STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES + sizeof(Ctrl) + 1024;
+static_assert(SMEM_FWD <= 232448, "shared memory budget of one CTA");
 constexpr size_t SMEM_BWD = STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES + sizeof(Ctrl) + 1024;
 static_assert(SMEM_BWD <= 232448, "shared memory budget of one CTA");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    k_fwd(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW, const FwdP p) {
+    k_fwd(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
+          const __grid_constant__ CUtensorMap tmE, const FwdP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  uint8_t* stg_base = base + STAGES * STAGE_BYTES;
+  Ctrl* c = reinterpret_cast<Ctrl*>(stg_base + NUM_EPI_WARPS * STG_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
   prologue(c, warp);
@@ -265,9 +271,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       const float mb2 = m * L2E;
       float s = 0.f;
+      const uint32_t stg = saddr(stg_base + (warp - 2) * STG_BYTES);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         if (g * 32 >= ncol) break;
+        if (p.E && (g & 1) == 0) {   // the staging block's previous contents have left
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
         uint32_t hv[16];
         if (ncol == 128) {
 #pragma unroll
@@ -288,10 +299,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
           }
         }
-        if (p.E && vrow) {
-          uint4* dst = reinterpret_cast<uint4*>(p.E + (int64_t)row * p.lde + c0 + g * 32);
+        if (p.E) {
+          // row `lane` of the warp's 32 x 64 block, 16-byte chunk k at chunk k ^ (lane % 8)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
+          for (int k = 0; k < 4; ++k)
+            sts128(stg + lane * 128 + ((((g & 1) * 4 + k) ^ (lane & 7)) << 4), hv[4 * k], hv[4 * k + 1],
+                   hv[4 * k + 2], hv[4 * k + 3]);
+          if ((g & 1) == 1 || (g + 1) * 32 >= ncol) {
+            // the block goes out by TMA; rows past the chunk and columns past V are clipped
+            // by the tensor map (the columns a half-filled block leaves are past V)
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmE, stg, (int)(c0 + (g >> 1) * 64), mp * 256 + (int)rank * 128 + q * 32);
+              bulk_commit();
+            }
+          }
         }
       }
       const int64_t tix = (int64_t)nb * 2 + h;
@@ -300,6 +323,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (p.gprev) side_run(p, sj, quota);
     }
     if (p.gprev && !c->abort) side_run(p, sj, INT64_MAX);   // what rounding left over
+    if (lane == 0) bulk_wait_all();   // every exp block has left shared memory and landed
+    __syncwarp();
   }
   teardown(c, warp);
 }
@@ -575,9 +600,16 @@ cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
   using namespace tc;
   if (!set_smem_attr()) return cudaErrorInvalidConfiguration;
   // boxes of 64 (K) x 128 rows: each CTA of a pair stages 128 rows of H and 128 of W
-  CUtensorMap mH, mW;
+  CUtensorMap mH, mW, mE;
   if (!make_map(&mH, a.H, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;
   if (!make_map(&mW, a.W, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;
+  // fp16 exp tile [rows, V] with row stride lde, stored in 64 x 32 blocks (a 16-bit map:
+  // the store copies the bits); statistics-only launches pass no E and use the H map
+  if (a.E) {
+    if (!make_map(&mE, a.E, (uint64_t)a.V, (uint64_t)a.rows, (uint64_t)a.lde, 64, 32)) return cudaErrorInvalidValue;
+  } else {
+    mE = mH;
+  }
   FwdP p;
   p.r0 = a.r0; p.rows = a.rows; p.V = a.V;
   p.mt = (a.rows + 255) / 256;
@@ -593,7 +625,7 @@ cudaError_t tc_forward(const TcFwdArgs& a, cudaStream_t s) {
   const int total = p.mt * p.ntn;
   int pairs = max_pairs((const void*)k_fwd, SMEM_FWD);
   if (pairs > total) pairs = total;
-  k_fwd<<<2 * pairs, NUM_THREADS, SMEM_FWD, s>>>(mH, mW, p);
+  k_fwd<<<2 * pairs, NUM_THREADS, SMEM_FWD, s>>>(mH, mW, mE, p);
   return cudaGetLastError();
 }
 
