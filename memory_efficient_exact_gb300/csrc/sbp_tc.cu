@@ -365,7 +365,7 @@ __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_bwd(const __grid_constant__ CUtensorMap tmGk, const __grid_constant__ CUtensorMap tmGmn,
           const __grid_constant__ CUtensorMap tmWmn, const __grid_constant__ CUtensorMap tmHmn,
-          const __grid_constant__ CUtensorMap tmDW, const BwdP p) {
+          const __grid_constant__ CUtensorMap tmDW, const __grid_constant__ CUtensorMap tmDH, const BwdP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg_base = base + STAGES * STAGE_BYTES;
@@ -507,16 +507,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
       const int64_t c0 = (int64_t)w.nb * BN + h * 128;
-      const int64_t row = (int64_t)w.mp * 256 + rank * 128 + lrow;
-      float* dst;
-      bool vrow;
-      if (w.kind == 0) {
-        vrow = row < p.rows;
-        dst = p.dh_part + ((int64_t)w.split * p.batch + w.z) * p.plane + row * p.d;
-      } else {
-        vrow = row < p.V;
-        dst = p.dW + row * p.d;
-      }
       uint32_t r[4][32];
       __syncwarp();
 #pragma unroll
@@ -553,22 +543,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      if (vrow) {
+      {
+        // dH split-K partial rows [y0, y0+32) x columns [cg, cg+32) of plane split * batch + z,
+        // through the same staging block and a TMA store (rows past the chunk and columns
+        // past d are clipped by the three-dimensional map)
+        const uint32_t stg = saddr(stg_base + (warp - 2) * STG_BYTES);
+        const int y0 = w.mp * 256 + (int)rank * 128 + q * 32;
+        const int zpl = w.split * p.batch + w.z;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int64_t cg = c0 + g * 32;
           if (cg >= p.d) break;
-          float* o = dst + cg;
-          if (cg + 32 <= p.d) {
-            float4* o4 = reinterpret_cast<float4*>(o);
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              o4[k] = make_float4(__uint_as_float(r[g][4 * k]), __uint_as_float(r[g][4 * k + 1]),
-                                  __uint_as_float(r[g][4 * k + 2]), __uint_as_float(r[g][4 * k + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (cg + j < p.d) o[j] = __uint_as_float(r[g][j]);
+          for (int k = 0; k < 8; ++k)
+            sts128(stg + lane * 128 + ((k ^ (lane & 7)) << 4), r[g][4 * k], r[g][4 * k + 1], r[g][4 * k + 2],
+                   r[g][4 * k + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0 && y0 < p.rows) {
+            tma_store_3d(&tmDH, stg, (int)cg, y0, zpl);
+            bulk_commit();
           }
         }
       }
@@ -642,8 +638,17 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   if (!make_map(&mGmn, a.G, (uint64_t)a.V, g_rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mWmn, a.W, (uint64_t)a.d, w_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mHmn, a.H, (uint64_t)a.d, h_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
-  CUtensorMap mDW;
+  CUtensorMap mDW, mDH;
   if (!make_map_f32(&mDW, a.dW, (uint64_t)a.d, dw_rows)) return cudaErrorInvalidValue;
+  // dH partials [splits * batch planes][rows][d] fp32: a 3-D map, so that stores clip at
+  // the chunk's last row of each plane
+  if (!a.dw_only && a.dh_part) {
+    if (!make_map3_f32(&mDH, a.dh_part, (uint64_t)a.d, (uint64_t)a.rows,
+                       (uint64_t)a.splits * (uint64_t)(a.batch > 0 ? a.batch : 1)))
+      return cudaErrorInvalidValue;
+  } else {
+    mDH = mDW;
+  }
   BwdP p;
   p.rows = a.rows; p.r0 = a.r0; p.V = a.V; p.d = a.d;
   p.mt_c = (a.rows + 255) / 256;
@@ -663,7 +668,7 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   p.counter = a.counter; p.status = a.status; p.limit_ns = wait_limit_ns();
   int pairs = max_pairs((const void*)k_bwd, SMEM_BWD);
   if (pairs > p.n_total) pairs = p.n_total;
-  k_bwd<<<2 * pairs, NUM_THREADS, SMEM_BWD, s>>>(mGk, mGmn, mWmn, mHmn, mDW, p);
+  k_bwd<<<2 * pairs, NUM_THREADS, SMEM_BWD, s>>>(mGk, mGmn, mWmn, mHmn, mDW, mDH, p);
   return cudaGetLastError();
 }
 
