@@ -42,10 +42,10 @@ PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T8192_d4096_V32768_chunk409
                         d=4096, V=32768, chunk=4096, dtype="bf16", seed=1002, mask="frac", frac=0.1)
 CPU_SAMPLE_TOKENS = 384
 # DRAM bytes (read + write) of one accumulating k_bwd launch, from an ncu capture of the
-# profile workload (d = 4096, chunk 4096, V = 32768: 2.444 GB read + 0.566 GB written),
+# profile workload (d = 4096, chunk 4096, V = 32768: 2.405 GB read + 0.566 GB written),
 # scaled to V = 151936 by the units processed (every operand but H_c grows with V).  Only
 # valid for the main workload's shape and the kernel version it was captured on.
-K_BWD_TRAFFIC_BYTES = (2.444e9 + 0.566e9) * 151936 / 32768
+K_BWD_TRAFFIC_BYTES = (2.405e9 + 0.566e9) * 151936 / 32768
 
 
 def load_peaks():
