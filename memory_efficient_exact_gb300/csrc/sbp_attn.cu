@@ -182,20 +182,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 cudaError_t tc_attn(const TcAttnArgs& a, bool ds, cudaStream_t s) {
   using namespace tc;
-  static int attr_done = 0;
+  static int attr_state[64] = {};
   static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    if (attr_done == 0) {
-      const bool ok =
-          cudaFuncSetAttribute(k_attn<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ATTN) ==
-              cudaSuccess &&
-          cudaFuncSetAttribute(k_attn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ATTN) ==
-              cudaSuccess;
-      attr_done = ok ? 1 : -1;
-    }
-    if (attr_done != 1) return cudaErrorInvalidConfiguration;
-  }
+  if (!once_per_device(attr_state, mu, [] {
+        return cudaFuncSetAttribute(k_attn<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ATTN) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(k_attn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ATTN) ==
+                   cudaSuccess;
+      }))
+    return cudaErrorInvalidConfiguration;
   // A: Q or dO, B: K or V, all [H * T, hd] row-major; boxes of 64 (hd) x 128 rows
   CUtensorMap mA, mB;
   const uint64_t rows_all = (uint64_t)a.H * (uint64_t)a.T;

@@ -891,17 +891,14 @@ bool map3_f32(CUtensorMap* m, void* ptr, int64_t T, int64_t H) {
 }
 
 bool fused_attrs() {
-  static int done = 0;
+  static int attr_state[64] = {};
   static std::mutex mu;
-  std::lock_guard<std::mutex> lk(mu);
-  if (done == 0) {
-    const bool ok = cudaFuncSetAttribute(tc::fa::k_attn_kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc::fa::SMEM_KV) == cudaSuccess &&
-                    cudaFuncSetAttribute(tc::fa::k_attn_q, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc::fa::SMEM_Q) == cudaSuccess;
-    done = ok ? 1 : -1;
-  }
-  return done == 1;
+  return tc::once_per_device(attr_state, mu, [] {
+    return cudaFuncSetAttribute(tc::fa::k_attn_kv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)tc::fa::SMEM_KV) == cudaSuccess &&
+           cudaFuncSetAttribute(tc::fa::k_attn_q, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)tc::fa::SMEM_Q) == cudaSuccess;
+  });
 }
 
 }  // namespace

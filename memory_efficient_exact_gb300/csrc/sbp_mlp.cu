@@ -25,10 +25,12 @@ struct MlpP {
 };
 
 // The epilogue's bf16 outputs leave through one 32 x 64 staging block (4 KB, 128-byte
-// swizzle) per warp and TMA stores: row-per-thread global stores (32 L2 sectors per
-// request) were measured to starve the operand loads.
+// swizzle) per warp and TMA stores, and k_mlp<true> reads g and u through the same block
+// with TMA loads (completing on one mbarrier per warp): row-per-thread global accesses
+// (32 L2 sectors per request) were measured to starve the operand loads.
 constexpr uint32_t STG_MLP = 32 * 64 * 2;
-constexpr size_t SMEM_MLP = STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_MLP + sizeof(Ctrl) + 1024;
+constexpr size_t SMEM_MLP =
+    STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_MLP + sizeof(Ctrl) + NUM_EPI_WARPS * sizeof(uint64_t) + 1024;
 static_assert(SMEM_MLP <= 232448, "shared memory budget of one CTA");
 
 // Row `lane` of a warp's staging block: 16-byte chunks k0 .. k0+3 from w (chunk k at
@@ -52,6 +54,35 @@ __device__ __forceinline__ void stage_free(int lane) {
   if (lane == 0) bulk_wait_read();
   __syncwarp();
 }
+// TMA load of a 32 x 64 block of `map` at column x, row y into this warp's staging block,
+// completing on the warp's mbarrier; waits for it (bounded) and returns whether it came.
+// The block's previous readers are this warp's lanes: their generic-proxy reads are
+// ordered before the asynchronous write by the proxy fence and the warp barrier.
+__device__ __forceinline__ bool stage_load(const CUtensorMap* map, uint32_t stg, uint64_t* bar, uint32_t& phase,
+                                           int lane, int x, int y, Ctrl* c, uint64_t limit) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    mbar_expect_tx(bar, STG_MLP);
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            stg),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
+        : "memory");
+  }
+  const bool ok = __all_sync(0xffffffffu, wait_bounded(bar, phase, &c->abort, limit));
+  phase ^= 1u;
+  return ok;
+}
+// Row `lane` of the warp's staging block (64 bf16 as 32 words), undoing the swizzle.
+__device__ __forceinline__ void stage_read_row(uint32_t stg, int lane, uint32_t (&w)[32]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4 * k]), "=r"(w[4 * k + 1]), "=r"(w[4 * k + 2]), "=r"(w[4 * k + 3])
+                 : "r"(stg + lane * 128 + ((k ^ (lane & 7)) << 4))
+                 : "memory");
+}
 constexpr uint32_t IDESC_KK = idesc_bf16(256, 256, false, false);
 constexpr uint32_t IDESC_KM = idesc_bf16(256, 256, false, true);
 
@@ -73,6 +104,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg_base = base + STAGES * STAGE_BYTES;
   Ctrl* c = reinterpret_cast<Ctrl*>(stg_base + NUM_EPI_WARPS * STG_MLP);
+  uint64_t* lbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(c) + sizeof(Ctrl));   // per epilogue warp
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
   prologue(c, warp);
@@ -149,6 +181,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int lrow = q * 32 + lane;
+    uint64_t* bar = lbar + (warp - 2);
+    uint32_t lphase = 0;
+    if (DA) {
+      if (lane == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      }
+      __syncwarp();
+    }
     int local = 0;
     for (int tile = pid; tile < total; tile += npairs, ++local) {
       const int mp = tile % p.mt, nb = tile / p.mt;
@@ -204,48 +245,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           stage_store(&tmGU, stg, lane, (t ? p.f : 0) + f0, yrow);
         }
       } else {
-        // this half tile's 128 columns of da in two 64-column blocks; dg and du replace
-        // g and u in place
-        __nv_bfloat16* gu = p.GU + (int64_t)row * 2 * p.f;
+        // this half tile's 128 columns of da in two 64-column blocks; g and u come in by TMA
+        // loads through the staging block, dg and du go out by TMA stores in their place
+        bool lok = true;
 #pragma unroll 1
-        for (int bx = 0; bx < 2; ++bx) {
+        for (int bx = 0; bx < 2 && lok; ++bx) {
           uint32_t r[2][32];
           tmem_ld32(tb + 128 * h + 64 * bx, r[0]);
           tmem_ld32(tb + 128 * h + 64 * bx + 32, r[1]);
           tmem_ld_wait();
           if (bx == 1) release_tmem(c, buf, lane);
           const int f0 = nb * BN + 128 * h + 64 * bx;
-          uint32_t duw[2][16];
+          uint32_t gw[32], uw[32];
           stage_free(lane);
+          lok = stage_load(&tmGU, stg, bar, lphase, lane, f0, yrow, c, p.limit_ns);
+          stage_read_row(stg, lane, gw);
+          lok = lok && stage_load(&tmGU, stg, bar, lphase, lane, (int)p.f + f0, yrow, c, p.limit_ns);
+          stage_read_row(stg, lane, uw);
+          if (!lok) break;
+          __syncwarp();
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            uint32_t dgw[16];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 G4 = make_uint4(0u, 0u, 0u, 0u), U4 = G4;
-              if (vrow) {
-                G4 = reinterpret_cast<const uint4*>(gu + f0 + 32 * g)[k];
-                U4 = reinterpret_cast<const uint4*>(gu + p.f + f0 + 32 * g)[k];
-              }
-              const uint32_t gw[4] = {G4.x, G4.y, G4.z, G4.w}, uw[4] = {U4.x, U4.y, U4.z, U4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 gg = unpack_bf16(gw[e]), uu = unpack_bf16(uw[e]);
-                const float a0 = __uint_as_float(r[g][8 * k + 2 * e]), a1 = __uint_as_float(r[g][8 * k + 2 * e + 1]);
-                const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
-                // dg = da u silu'(g), silu'(g) = s (1 + g (1 - s));  du = da silu(g)
-                dgw[4 * k + e] = pack_bf16(a0 * uu.x * s0 * (1.f + gg.x * (1.f - s0)),
-                                           a1 * uu.y * s1 * (1.f + gg.y * (1.f - s1)));
-                duw[g][4 * k + e] = pack_bf16(a0 * gg.x * s0, a1 * gg.y * s1);
-              }
-            }
-            stage4(stg, lane, 4 * g, dgw);
+          for (int w = 0; w < 32; ++w) {   // dg replaces g, du replaces u (word by word)
+            const float2 gg = unpack_bf16(gw[w]), uu = unpack_bf16(uw[w]);
+            const float a0 = __uint_as_float(r[w >> 4][(2 * w) & 31]), a1 = __uint_as_float(r[w >> 4][(2 * w + 1) & 31]);
+            const float s0 = sigmoid_fast(gg.x), s1 = sigmoid_fast(gg.y);
+            // dg = da u silu'(g), silu'(g) = s (1 + g (1 - s));  du = da silu(g)
+            gw[w] = pack_bf16(a0 * uu.x * s0 * (1.f + gg.x * (1.f - s0)), a1 * uu.y * s1 * (1.f + gg.y * (1.f - s1)));
+            uw[w] = pack_bf16(a0 * gg.x * s0, a1 * gg.y * s1);
           }
+          // the staging block holds u (read by every lane above): dg replaces it
+          stage4(stg, lane, 0, gw);
+          stage4(stg, lane, 4, gw + 16);
           stage_store(&tmGU, stg, lane, f0, yrow);
           stage_free(lane);
-          stage4(stg, lane, 0, duw[0]);
-          stage4(stg, lane, 4, duw[1]);
-          stage_store(&tmGU, stg, lane, p.f + f0, yrow);
+          stage4(stg, lane, 0, uw);
+          stage4(stg, lane, 4, uw + 16);
+          stage_store(&tmGU, stg, lane, (int)p.f + f0, yrow);
+        }
+        if (!lok) {
+          fail(c, p.status);
+          break;
         }
       }
     }
@@ -259,20 +298,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 cudaError_t tc_mlp(const TcMlpArgs& a, bool da, cudaStream_t s) {
   using namespace tc;
-  static int attr_done = 0;
+  static int attr_state[64] = {};
   static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    if (attr_done == 0) {
-      const bool ok =
-          cudaFuncSetAttribute(k_mlp<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MLP) ==
-              cudaSuccess &&
-          cudaFuncSetAttribute(k_mlp<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MLP) ==
-              cudaSuccess;
-      attr_done = ok ? 1 : -1;
-    }
-    if (attr_done != 1) return cudaErrorInvalidConfiguration;
-  }
+  if (!once_per_device(attr_state, mu, [] {
+        return cudaFuncSetAttribute(k_mlp<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MLP) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(k_mlp<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MLP) ==
+                   cudaSuccess;
+      }))
+    return cudaErrorInvalidConfiguration;
   CUtensorMap mA, mB;
   // A: x or dY rows [T, d], boxes of 64 (K) x 128 rows
   if (!make_map(&mA, a.Arows, (uint64_t)a.d, (uint64_t)a.T, (uint64_t)a.d, BK, 128)) return cudaErrorInvalidValue;

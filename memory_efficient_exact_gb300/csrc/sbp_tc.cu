@@ -578,16 +578,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // ======================================================================================= host
 
 bool set_smem_attr() {
-  static int done = 0;  // 1 ok, -1 failed
+  static int attr_state[64] = {};
   static std::mutex mu;
-  std::lock_guard<std::mutex> lk(mu);
-  if (done == 0) {
-    const bool ok =
-        cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_FWD) == cudaSuccess &&
-        cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BWD) == cudaSuccess;
-    done = ok ? 1 : -1;
-  }
-  return done == 1;
+  return once_per_device(attr_state, mu, [] {
+    return cudaFuncSetAttribute(k_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_FWD) == cudaSuccess &&
+           cudaFuncSetAttribute(k_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BWD) == cudaSuccess;
+  });
 }
 
 }  // namespace tc

@@ -391,6 +391,18 @@ inline uint64_t wait_limit_ns() {
   return v;
 }
 
+// Runs `set` (the cudaFuncSetAttribute calls of one kernel family) once for the current
+// device: function attributes are per device, so a process driving several GPUs sets
+// them on each.  Returns whether they are set.
+template <class F>
+inline bool once_per_device(int (&state)[64], std::mutex& mu, F set) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (state[dev] == 0) state[dev] = set() ? 1 : -1;
+  return state[dev] == 1;
+}
+
 // Clusters of two (SM pairs) of `kernel` that can be resident at once, cached per
 // device and kernel.
 inline int max_pairs(const void* kernel, size_t smem_bytes, int threads = NUM_THREADS) {
