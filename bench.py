@@ -217,7 +217,8 @@ def run_ours(args):
     Ht = torch.from_numpy(H).to(dev).to(torch.bfloat16)
     Wt = torch.from_numpy(W).to(dev).to(torch.bfloat16)
     yt = torch.from_numpy(y).to(dev)
-    ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT, dev)
+    lean = bool(getattr(args, "lean", False))
+    ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT, dev, lean=lean)
     dH = torch.empty_like(Ht)
     dW = torch.empty((V, d), dtype=torch.float32, device=dev)
     st = torch.zeros((), dtype=torch.int32, device=dev)
@@ -231,7 +232,7 @@ def run_ours(args):
         n_resp = max(1, T // 2048)
         At = torch.from_numpy(I.make_advantages(n_resp, (T + n_resp - 1) // n_resp, w["seed"])[:T]).to(dev)
         lpo = torch.from_numpy((-12.8 + I.make_logp_noise(T, w["seed"])).astype("float32")).to(dev)
-        ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_GRPO, dev)
+        ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_GRPO, dev, lean=lean)
 
         def step():
             return sbp.grpo(Ht, Wt, yt, At, lpo, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False,
@@ -241,7 +242,7 @@ def run_ours(args):
         n_seq = max(2, T // 4096)
         cu = torch.from_numpy(I.cu_seqlens(n_seq, T // n_seq)).to(dev)
         sref = torch.from_numpy(I.make_ref_seq_logp(n_seq, w["seed"])).to(dev)
-        ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_DPO2, dev)
+        ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_DPO2, dev, lean=lean)
 
         def step():
             p1 = sbp.dpo_pass1(Ht, Wt, yt, cu, chunk, workspace=ws, status=st, logp=False, stream=stream)
@@ -365,6 +366,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w["workload"], "objective": objective, "T": T, "d": d, "V": V, "chunk": chunk,
+                   "schedule": "one chunk buffer" if lean else "two chunk buffers",
                    "tokens_per_gpu_per_step": T, "ignored_frac": w["frac"],
                    "l2": f"inputs larger than L2 (W {V * d * 2 / 1e9:.2f} GB; chunk logits "
                          f"{chunk * V * 2 / 1e9:.2f} GB per chunk)",
@@ -634,6 +636,8 @@ def main(argv=None):
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
     ap.add_argument("--hd", type=int, default=None, help="override the attention head width (--sublayer attn)")
+    ap.add_argument("--lean", action="store_true",
+                    help="LM head: the smallest workspace (one chunk buffer, gradient as its own pass)")
     ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
     ap.add_argument("--sublayer", choices=["lmhead", "mlp", "attn"], default="lmhead",
                     help="mlp / attn: the chunked SwiGLU-MLP or causal-attention backward (own JSON line)")

@@ -75,11 +75,23 @@ extern "C" {
 #define SBP_MODE_DPO1 2
 #define SBP_MODE_DPO2 3
 
-/* Bytes of workspace the call with these arguments needs.  It depends on T only
- * through O(T) scalars; the bulk is one chunk's logits/gradient (chunk x V) plus
- * chunk x d split partials.  Returns 0 for invalid arguments. */
+/* Bytes of workspace the call with these arguments needs for the fastest schedule.  It
+ * depends on T only through O(T) scalars; the bulk is the chunk logits/gradient buffers
+ * (chunk x V each) plus chunk x d split partials.  bf16 calls that form a gradient over
+ * more than one chunk get two chunk buffers: chunk c's logit gradient is then formed by
+ * the epilogue warps of chunk c+1's forward GEMM instead of by a separate pass.
+ * Returns 0 for invalid arguments. */
 size_t sbp_lmhead_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t chunk,
                                   int dtype, int mode);
+
+/* The smallest workspace the call accepts: one chunk buffer (chunk x V x 2 bytes less
+ * than sbp_lmhead_workspace_bytes where that one has two).  A workspace of at least
+ * this size but below sbp_lmhead_workspace_bytes selects the one-buffer schedule, in
+ * which each chunk's logit gradient runs as its own pass (a few percent slower, same
+ * results bit for bit).  Equal to sbp_lmhead_workspace_bytes where that one has one
+ * buffer.  Returns 0 for invalid arguments. */
+size_t sbp_lmhead_workspace_bytes_lean(int64_t T, int64_t d, int64_t V, int64_t chunk,
+                                       int dtype, int mode);
 
 /* SFT cross-entropy (ziziman.com article, LM-head paragraph on SFT/GRPO):
  *   L = -(1/N) sum_{t: y_t != ign} logp_t,   logp_t = Z_{t,y_t} - logsumexp_v Z_{t,v}.

@@ -472,6 +472,12 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 
 int validate(const Call& c, Layout* L) {
   if (!make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, L, c.nbuf)) return SBP_ERR_INVALID_ARG;
+  // a workspace too small for the default two chunk buffers but large enough for one
+  // selects the one-buffer schedule (the logit gradient as its own pass per chunk)
+  if (c.nbuf == 0 && L->nbuf == 2 && c.ws_bytes < L->total) {
+    Layout lean;
+    if (make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, &lean, 1) && c.ws_bytes >= lean.total) *L = lean;
+  }
   if (c.T > 0 && (!c.H || !c.labels)) return SBP_ERR_INVALID_ARG;
   if (!c.W || !c.dev_status) return SBP_ERR_INVALID_ARG;
   if (c.T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
@@ -1033,6 +1039,12 @@ extern "C" {
 size_t sbp_lmhead_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode) {
   Layout L;
   if (!make_layout(T, d, V, chunk, dtype, mode, &L)) return 0;
+  return L.total;
+}
+
+size_t sbp_lmhead_workspace_bytes_lean(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode) {
+  Layout L;
+  if (!make_layout(T, d, V, chunk, dtype, mode, &L, 1)) return 0;
   return L.total;
 }
 

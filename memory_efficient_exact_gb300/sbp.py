@@ -41,6 +41,8 @@ def _load() -> ctypes.CDLL:
     C = ctypes.c_int
     lib.sbp_lmhead_workspace_bytes.restype = SZ
     lib.sbp_lmhead_workspace_bytes.argtypes = [I64, I64, I64, I64, C, C]
+    lib.sbp_lmhead_workspace_bytes_lean.restype = SZ
+    lib.sbp_lmhead_workspace_bytes_lean.argtypes = [I64, I64, I64, I64, C, C]
     lib.sbp_lmhead_sft.restype = C
     lib.sbp_lmhead_sft.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, SZ, P, P]
     lib.sbp_lmhead_grpo.restype = C
@@ -114,6 +116,11 @@ def workspace_bytes(T: int, d: int, V: int, chunk: int, dtype: int, mode: int) -
     return int(_lib.sbp_lmhead_workspace_bytes(T, d, V, chunk, dtype, mode))
 
 
+def workspace_bytes_lean(T: int, d: int, V: int, chunk: int, dtype: int, mode: int) -> int:
+    """The smallest accepted workspace (one chunk buffer: the one-buffer schedule)."""
+    return int(_lib.sbp_lmhead_workspace_bytes_lean(T, d, V, chunk, dtype, mode))
+
+
 def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -142,8 +149,8 @@ def _check(code: int, where: str):
         raise SbpError(code, where)
 
 
-def make_workspace(T, d, V, chunk, dtype, mode, device=None) -> torch.Tensor:
-    n = workspace_bytes(T, d, V, chunk, dtype, mode)
+def make_workspace(T, d, V, chunk, dtype, mode, device=None, lean=False) -> torch.Tensor:
+    n = (workspace_bytes_lean if lean else workspace_bytes)(T, d, V, chunk, dtype, mode)
     if n == 0:
         raise SbpError(ERR_INVALID_ARG, "workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")

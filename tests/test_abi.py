@@ -40,6 +40,22 @@ def test_status_strings(sbp):
     assert sbp.status_string(99) == "SBP_ERR_UNKNOWN"
 
 
+def test_lean_workspace(sbp):
+    # two chunk buffers by default for multi-chunk bf16 gradients; the lean size has one
+    d, V = 4096, 151936
+    full = sbp.workspace_bytes(16384, d, V, 4096, sbp.BF16, sbp.MODE_SFT)
+    lean = sbp.workspace_bytes_lean(16384, d, V, 4096, sbp.BF16, sbp.MODE_SFT)
+    assert full - lean >= 4096 * V * 2 and lean > 4096 * V * 2
+    # one chunk, DPO pass 1 and fp32 have one buffer either way
+    assert sbp.workspace_bytes_lean(4096, d, V, 4096, sbp.BF16, sbp.MODE_SFT) == \
+        sbp.workspace_bytes(4096, d, V, 4096, sbp.BF16, sbp.MODE_SFT)
+    assert sbp.workspace_bytes_lean(16384, d, V, 4096, sbp.BF16, sbp.MODE_DPO1) == \
+        sbp.workspace_bytes(16384, d, V, 4096, sbp.BF16, sbp.MODE_DPO1)
+    assert sbp.workspace_bytes_lean(256, 64, 1000, 64, sbp.FP32, sbp.MODE_SFT) == \
+        sbp.workspace_bytes(256, 64, 1000, 64, sbp.FP32, sbp.MODE_SFT)
+    assert sbp.workspace_bytes_lean(16, 0, 10, 4, sbp.BF16, 0) == 0
+
+
 def test_workspace_bytes(sbp):
     V, d = 151936, 4096
     w1 = sbp.workspace_bytes(16384, d, V, 2048, sbp.BF16, sbp.MODE_SFT)

@@ -169,6 +169,30 @@ def test_accumulate_dw_and_determinism(sbp, dtype):
     assert torch.allclose(acc, 2 * a["dW"], rtol=1e-6, atol=1e-9)
 
 
+def test_lean_workspace_same_bits(sbp):
+    # the one-buffer schedule (the smallest workspace) forms each chunk's logit gradient
+    # in its own pass instead of inside the next chunk's forward: same arithmetic, so the
+    # same bits, for SFT and GRPO over several chunks
+    T, d, V, chunk = 700, 256, 3000, 128
+    H, W, y = make_case(T, d, V, "bf16", seed=11, w_std=0.08)
+    Ht, Wt, yt = to_dev(torch, H, W, y, "bf16")
+    lean = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT, lean=True)
+    assert lean.numel() < sbp.workspace_bytes(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT)
+    a = sbp.sft(Ht, Wt, yt, chunk)
+    b = sbp.sft(Ht, Wt, yt, chunk, workspace=lean)
+    adv = torch.from_numpy(I.make_advantages(T // 4, 4, 11)).cuda()
+    lpo = torch.randn(T, device="cuda") * 0.1 - 8.0
+    c = sbp.grpo(Ht, Wt, yt, adv, lpo, chunk)
+    e = sbp.grpo(Ht, Wt, yt, adv, lpo, chunk, workspace=lean)
+    torch.cuda.synchronize()
+    sbp.check_status(b["status"])
+    for x, z in ((a, b), (c, e)):
+        assert torch.equal(x["dH"], z["dH"]) and torch.equal(x["dW"], z["dW"]) and torch.equal(x["loss"], z["loss"])
+    small = torch.empty(lean.numel() - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sbp.SbpError):
+        sbp.sft(Ht, Wt, yt, chunk, workspace=small)
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_edge_cases(sbp, dtype):
     d, V = 64, 512
