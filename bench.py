@@ -609,6 +609,14 @@ def run_attn_bench(args):
         "executed_tflops": flops * args.steps / (ms / 1000.0) / 1e12,
         "pct_bf16_peak": 100.0 * flops * args.steps / (ms / 1000.0) / 1e12 / peaks["bf16_tflops"],
         "chunk_buffer_gbs": pds_bytes * args.steps / (ms / 1000.0) / 1e9 if pds_bytes else None,
+        # the dominant kernel of the path against the tensor roofline (its own GEMMs)
+        "roofline": {"kernel": names[0] if sp_ms >= bw_ms else names[1], "bound": "tensor",
+                     "achieved": (2 * gemms[0] * hd * H * rowkeys * args.steps / (sp_ms / 1000.0) / 1e12
+                                  if sp_ms >= bw_ms else
+                                  2 * gemms[1] * hd * H * rowkeys * args.steps / (bw_ms / 1000.0) / 1e12)
+                     if (sp_n and bw_n) else None,
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s", "traffic": None,
+                     "peak_source": f"bf16 dense, sustained, {src}"},
         "kernels": {names[0]: {"ms": sp_ms, "launches": sp_n,
                                "tflops": 2 * gemms[0] * hd * H * rowkeys * args.steps / (sp_ms / 1000.0) / 1e12
                                if sp_n else None},
@@ -620,6 +628,8 @@ def run_attn_bench(args):
         "unchunked_scores_gb": H * T * T * 2 * 2 / 1e9,
         "gpu_launches": launches * args.steps, "clocks": clk,
     }
+    rf = line["roofline"]
+    rf["frac"] = rf["achieved"] / rf["peak"] if rf["achieved"] else None
     print(json.dumps(line), flush=True)
     return 0
 

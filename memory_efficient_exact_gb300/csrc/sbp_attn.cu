@@ -26,15 +26,24 @@ struct AttnP {
   int32_t* status; uint64_t limit_ns;
 };
 
-constexpr size_t SMEM_ATTN = STAGES * STAGE_BYTES + sizeof(Ctrl) + 1024;
+// P and dS leave through one 32 x 64 bf16 staging block per epilogue warp and TMA stores
+// (k_attn<true> reads P back the same way, by TMA loads completing on a per-warp
+// mbarrier): row-per-thread global accesses were measured to starve the operand loads.
+constexpr uint32_t STG_ATTN = 32 * 64 * 2;
+constexpr size_t SMEM_ATTN =
+    STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_ATTN + sizeof(Ctrl) + NUM_EPI_WARPS * sizeof(uint64_t) + 1024;
+static_assert(SMEM_ATTN <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t IDESC_ATTN = idesc_bf16(256, 256, false, false);
 
 template <bool DS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    k_attn(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const AttnP p) {
+    k_attn(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmDS, const AttnP p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl* c = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  uint8_t* stg_base = base + STAGES * STAGE_BYTES;
+  Ctrl* c = reinterpret_cast<Ctrl*>(stg_base + NUM_EPI_WARPS * STG_ATTN);
+  uint64_t* lbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(c) + sizeof(Ctrl));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
   prologue(c, warp);
@@ -106,74 +115,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int lrow = q * 32 + lane;
     const float sl2 = p.scale * L2E;
+    const uint32_t stg = saddr(stg_base + (warp - 2) * STG_ATTN);
+    uint64_t* bar = lbar + (warp - 2);
+    uint32_t lphase = 0;
+    if (DS) {
+      if (lane == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      }
+      __syncwarp();
+    }
     int local = 0;
-    for (int tile = pid; tile < total; tile += npairs, ++local) {
+    bool ok = true;
+    for (int tile = pid; tile < total && ok; tile += npairs, ++local) {
       const int z = tile / per_head, rem = tile % per_head;
       const int mp = rem % p.mt, nb = rem / p.mt;
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      const int row = mp * 256 + (int)rank * 128 + lrow;   // within the chunk
+      const int row = mp * 256 + (int)rank * 128 + lrow;   // within the chunk (< Cmax)
       if (!warp_wait_cluster(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
         fail(c, p.status);
         break;
       }
       tc_fence_after();
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + h * 128);
-      uint32_t r[4][32];
       __syncwarp();
-#pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld32(tb + g * 32, r[g]);
-      tmem_ld_wait();
-      release_tmem(c, buf, lane);
-      if (row >= p.Cmax) continue;
       const int64_t j0 = (int64_t)nb * BN + h * 128;        // first key of this thread's 128
-      const int64_t off = ((int64_t)z * p.Cmax + row) * p.Lp + j0;
-      uint4* out = reinterpret_cast<uint4*>((DS ? p.dS : p.P) + off);
-      if (row >= p.rows) {                                   // padding rows read as zero
-#pragma unroll
-        for (int k = 0; k < 16; ++k) out[k] = make_uint4(0u, 0u, 0u, 0u);
-        continue;
-      }
+      const int yrow = (int)(z * p.Cmax) + mp * 256 + (int)rank * 128 + q * 32;   // the warp's first row
+      const bool vrow = row < p.rows;                        // padding rows are written as zero
       const int64_t t = p.c0 + row;                          // query position
-      if (!DS) {
-        const float lz = p.lse[z * p.T + t] * L2E;
+      const float lz = (!DS && vrow) ? p.lse[z * p.T + t] * L2E : 0.f;
+      const float Dt = (DS && vrow) ? p.D[z * p.T + t] : 0.f;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+      for (int bx = 0; bx < 2; ++bx) {   // two 64-key blocks of the warp's 128
+        uint32_t r[2][32];
+        tmem_ld32(tb + 64 * bx, r[0]);
+        tmem_ld32(tb + 64 * bx + 32, r[1]);
+        tmem_ld_wait();
+        if (bx == 1) release_tmem(c, buf, lane);
+        stage_free(lane);
+        uint32_t pin[32];
+        if (DS) {
+          if (!stage_load(&tmP, stg, STG_ATTN, bar, lphase, lane, (int)(j0 + 64 * bx), yrow, c, p.limit_ns)) {
+            fail(c, p.status);
+            ok = false;
+            break;
+          }
+          stage_read_row(stg, lane, pin);
+          __syncwarp();
+        }
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          const int g = 2 * bx + gg;
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const int64_t key = j0 + g * 32 + j;
-            const float p0 = key <= t ? ex2(fmaf(__uint_as_float(r[g][j]), sl2, -lz)) : 0.f;
-            const float p1 = key + 1 <= t ? ex2(fmaf(__uint_as_float(r[g][j + 1]), sl2, -lz)) : 0.f;
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            float v0 = 0.f, v1 = 0.f;
+            if (vrow) {
+              if (!DS) {
+                const int64_t key = j0 + g * 32 + j;
+                v0 = key <= t ? ex2(fmaf(__uint_as_float(r[gg][j]), sl2, -lz)) : 0.f;
+                v1 = key + 1 <= t ? ex2(fmaf(__uint_as_float(r[gg][j + 1]), sl2, -lz)) : 0.f;
+              } else {
+                const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pin[16 * gg + j / 2]);
+                const float2 pp = __bfloat1622float2(pb);
+                v0 = p.scale * pp.x * (__uint_as_float(r[gg][j]) - Dt);
+                v1 = p.scale * pp.y * (__uint_as_float(r[gg][j + 1]) - Dt);
+              }
+            }
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
             pk[j / 2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) out[4 * g + k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          stage4(stg, lane, 4 * gg, pk);
         }
-      } else {
-        const float Dt = p.D[z * p.T + t];
-        const uint4* pin = reinterpret_cast<const uint4*>(p.P + off);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 P4 = pin[4 * g + k];
-            const uint32_t pw[4] = {P4.x, P4.y, P4.z, P4.w};
-            uint32_t ow[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 pp = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[e]));
-              const float d0 = __uint_as_float(r[g][8 * k + 2 * e]), d1 = __uint_as_float(r[g][8 * k + 2 * e + 1]);
-              const __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(p.scale * pp.x * (d0 - Dt), p.scale * pp.y * (d1 - Dt));
-              ow[e] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            out[4 * g + k] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-          }
-        }
+        stage_store(DS ? &tmDS : &tmP, stg, lane, (int)(j0 + 64 * bx), yrow);
       }
     }
+    if (lane == 0) bulk_wait_all();   // every block has left shared memory and landed
+    __syncwarp();
   }
   teardown(c, warp);
 }
@@ -207,11 +226,16 @@ cudaError_t tc_attn(const TcAttnArgs& a, bool ds, cudaStream_t s) {
   p.Cmax = a.Cmax; p.Lp = a.Lp;
   p.status = a.status; p.limit_ns = wait_limit_ns();
   const int total = p.mt * p.ntn * p.H;
+  // P and dS: [H * Cmax, Lp] bf16, 64 x 32 blocks
+  CUtensorMap mP, mDS;
+  const uint64_t prow = (uint64_t)a.H * (uint64_t)a.Cmax;
+  if (!make_map(&mP, a.P, (uint64_t)a.Lp, prow, (uint64_t)a.Lp, 64, 32)) return cudaErrorInvalidValue;
+  if (!make_map(&mDS, a.dS, (uint64_t)a.Lp, prow, (uint64_t)a.Lp, 64, 32)) return cudaErrorInvalidValue;
   const void* kern = ds ? (const void*)k_attn<true> : (const void*)k_attn<false>;
   int pairs = max_pairs(kern, SMEM_ATTN);
   if (pairs > total) pairs = total;
-  if (ds) k_attn<true><<<2 * pairs, NUM_THREADS, SMEM_ATTN, s>>>(mA, mB, p);
-  else k_attn<false><<<2 * pairs, NUM_THREADS, SMEM_ATTN, s>>>(mA, mB, p);
+  if (ds) k_attn<true><<<2 * pairs, NUM_THREADS, SMEM_ATTN, s>>>(mA, mB, mP, mDS, p);
+  else k_attn<false><<<2 * pairs, NUM_THREADS, SMEM_ATTN, s>>>(mA, mB, mP, mDS, p);
   return cudaGetLastError();
 }
 

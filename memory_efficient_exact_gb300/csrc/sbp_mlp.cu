@@ -33,69 +33,6 @@ constexpr size_t SMEM_MLP =
     STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_MLP + sizeof(Ctrl) + NUM_EPI_WARPS * sizeof(uint64_t) + 1024;
 static_assert(SMEM_MLP <= 232448, "shared memory budget of one CTA");
 
-// Row `lane` of a warp's staging block: 16-byte chunks k0 .. k0+3 from w (chunk k at
-// chunk k ^ (lane % 8)).
-__device__ __forceinline__ void stage4(uint32_t stg, int lane, int k0, const uint32_t* w) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    sts128(stg + lane * 128 + (((k0 + k) ^ (lane & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-}
-// Hands the staging block to TMA (store at column x, row y of `map`) once the previous
-// contents have been read out; the next write must wait for this one to be read.
-__device__ __forceinline__ void stage_store(const CUtensorMap* map, uint32_t stg, int lane, int x, int y) {
-  fence_proxy_async();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_2d(map, stg, x, y);
-    bulk_commit();
-  }
-}
-__device__ __forceinline__ void stage_free(int lane) {
-  if (lane == 0) bulk_wait_read();
-  __syncwarp();
-}
-// TMA load of a 32 x 64 block of `map` at column x, row y into this warp's staging block,
-// completing on the warp's mbarrier; waits for it (bounded) and returns whether it came.
-// The block's previous readers are this warp's lanes: their generic-proxy reads are
-// ordered before the asynchronous write by the proxy fence and the warp barrier.
-__device__ __forceinline__ bool stage_load(const CUtensorMap* map, uint32_t stg, uint64_t* bar, uint32_t& phase,
-                                           int lane, int x, int y, Ctrl* c, uint64_t limit) {
-  fence_proxy_async();
-  __syncwarp();
-  if (lane == 0) {
-    mbar_expect_tx(bar, STG_MLP);
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            stg),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
-        : "memory");
-  }
-  const bool ok = __all_sync(0xffffffffu, wait_bounded(bar, phase, &c->abort, limit));
-  phase ^= 1u;
-  return ok;
-}
-// Row `lane` of the warp's staging block (64 bf16 as 32 words), undoing the swizzle.
-__device__ __forceinline__ void stage_read_row(uint32_t stg, int lane, uint32_t (&w)[32]) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[4 * k]), "=r"(w[4 * k + 1]), "=r"(w[4 * k + 2]), "=r"(w[4 * k + 3])
-                 : "r"(stg + lane * 128 + ((k ^ (lane & 7)) << 4))
-                 : "memory");
-}
-constexpr uint32_t IDESC_KK = idesc_bf16(256, 256, false, false);
-constexpr uint32_t IDESC_KM = idesc_bf16(256, 256, false, true);
-
-__device__ __forceinline__ float sigmoid_fast(float t) { return __fdividef(1.f, 1.f + ex2(-t * L2E)); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-}
-
 template <bool DA>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_mlp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -258,9 +195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const int f0 = nb * BN + 128 * h + 64 * bx;
           uint32_t gw[32], uw[32];
           stage_free(lane);
-          lok = stage_load(&tmGU, stg, bar, lphase, lane, f0, yrow, c, p.limit_ns);
+          lok = stage_load(&tmGU, stg, STG_MLP, bar, lphase, lane, f0, yrow, c, p.limit_ns);
           stage_read_row(stg, lane, gw);
-          lok = lok && stage_load(&tmGU, stg, bar, lphase, lane, (int)p.f + f0, yrow, c, p.limit_ns);
+          lok = lok && stage_load(&tmGU, stg, STG_MLP, bar, lphase, lane, (int)p.f + f0, yrow, c, p.limit_ns);
           stage_read_row(stg, lane, uw);
           if (!lok) break;
           __syncwarp();
