@@ -101,3 +101,75 @@ def test_row_and_column_functions_match_the_full_backward():
         dK, dV = A.keys_dKdV(Q, K, V, f["O"], dO, f["lse"], s, h, keys)
         np.testing.assert_allclose(dK, b["dK"][h, keys], rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(dV, b["dV"][h, keys], rtol=1e-12, atol=1e-13)
+
+
+def test_gqa_equals_mha_with_repeated_heads():
+    # grouped-query attention is multi-head attention with each key / value head repeated
+    # over its group; dK, dV of a shared head are the sums over the group (chain rule)
+    g = np.random.default_rng(21)
+    H, Hkv, T, hd, s = 6, 2, 9, 4, 0.5
+    Q, dO = g.standard_normal((H, T, hd)), g.standard_normal((H, T, hd))
+    K, V = g.standard_normal((Hkv, T, hd)), g.standard_normal((Hkv, T, hd))
+    Kr, Vr = np.repeat(K, H // Hkv, axis=0), np.repeat(V, H // Hkv, axis=0)
+    f, fr = A.forward(Q, K, V, s), A.forward(Q, Kr, Vr, s)
+    np.testing.assert_allclose(f["O"], fr["O"], rtol=1e-13, atol=1e-14)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+    br = A.backward(Q, Kr, Vr, fr["O"], dO, fr["lse"], s)
+    np.testing.assert_allclose(b["dQ"], br["dQ"], rtol=1e-12, atol=1e-13)
+    for key in ("dK", "dV"):
+        summed = br[key].reshape(Hkv, H // Hkv, T, hd).sum(axis=1)
+        np.testing.assert_allclose(b[key], summed, rtol=1e-12, atol=1e-13)
+    c = A.backward_chunked(Q, K, V, f["O"], dO, f["lse"], s, 4)
+    for key in ("dQ", "dK", "dV"):
+        np.testing.assert_allclose(c[key], b[key], rtol=1e-12, atol=1e-13)
+    dK, dV = A.keys_dKdV(Q, K, V, f["O"], dO, f["lse"], s, 1, [0, 4, 8])
+    np.testing.assert_allclose(dK, b["dK"][1, [0, 4, 8]], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dV, b["dV"][1, [0, 4, 8]], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(A.rows_dQ(Q, K, V, f["O"], dO, f["lse"], s, 5, [0, 8]), b["dQ"][5, [0, 8]],
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_gqa_matches_torch_sdpa_autograd_fp64():
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(22)
+    H, Hkv, T, hd, s = 4, 1, 8, 5, 0.4
+    Q, dO = g.standard_normal((H, T, hd)), g.standard_normal((H, T, hd))
+    K, V = g.standard_normal((Hkv, T, hd)), g.standard_normal((Hkv, T, hd))
+    f = A.forward(Q, K, V, s)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+    q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    try:
+        o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True, scale=s,
+                                                             enable_gqa=True)[0]
+    except TypeError:
+        pytest.skip("this torch has no grouped-query scaled_dot_product_attention")
+    o.backward(torch.tensor(dO))
+    np.testing.assert_allclose(f["O"], o.detach().numpy(), rtol=1e-12, atol=1e-13)
+    for t, key in ((q, "dQ"), (k, "dK"), (v, "dV")):
+        np.testing.assert_allclose(b[key], t.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_gqa_finite_differences():
+    g = np.random.default_rng(23)
+    H, Hkv, T, hd, s = 4, 2, 5, 3, 0.7
+    Q, dO = g.standard_normal((H, T, hd)), g.standard_normal((H, T, hd))
+    K, V = g.standard_normal((Hkv, T, hd)), g.standard_normal((Hkv, T, hd))
+    f = A.forward(Q, K, V, s)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+
+    def loss():
+        return float((A.forward(Q, K, V, s)["O"] * dO).sum())
+
+    for X, key in ((K, "dK"), (V, "dV")):
+        G = np.zeros_like(X)
+        it = np.nditer(X, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            old = X[i]
+            X[i] = old + 1e-6
+            lp = loss()
+            X[i] = old - 1e-6
+            lm = loss()
+            X[i] = old
+            G[i] = (lp - lm) / 2e-6
+        np.testing.assert_allclose(b[key], G, rtol=1e-6, atol=1e-8)
