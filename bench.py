@@ -520,17 +520,18 @@ ATTN_METRIC = "attention bwd tokens/s (causal, H=32, hd=128, T=8192)"
 
 def attn_forward_inputs(torch, Q, K, V, scale):
     """O and the row log-sum-exp of the causal forward, head by head in fp32 (input set-up
-    with plain torch ops, outside the timed region)."""
+    with plain torch ops, outside the timed region); K, V may have H / group heads."""
     H, T, hd = Q.shape
+    grp = H // K.shape[0]
     O = torch.empty_like(Q)
     lse = torch.empty((H, T), dtype=torch.float32, device=Q.device)
     mask = torch.ones((T, T), dtype=torch.bool, device=Q.device).triu(1)
     for h in range(H):
-        S = (Q[h].float() @ K[h].float().T) * scale
+        S = (Q[h].float() @ K[h // grp].float().T) * scale
         S.masked_fill_(mask, float("-inf"))
         l = torch.logsumexp(S, dim=1)
         lse[h] = l
-        O[h] = (torch.exp(S - l[:, None]) @ V[h].float()).to(Q.dtype)
+        O[h] = (torch.exp(S - l[:, None]) @ V[h // grp].float()).to(Q.dtype)
     return O, lse
 
 
@@ -548,15 +549,17 @@ def run_attn_bench(args):
     if args.hd:
         w["hd"] = args.hd
     H, T, hd, chunk = w["H"], w["T"], w["hd"], w["chunk"]
+    Hkv = args.kv_heads or H
     dev = torch.device("cuda", torch.cuda.current_device())
     g = torch.Generator(device=dev).manual_seed(w["seed"])
-    Q, K, V, dO = (torch.randn((H, T, hd), device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    Q, dO = (torch.randn((H, T, hd), device=dev, generator=g).to(torch.bfloat16) for _ in range(2))
+    K, V = (torch.randn((Hkv, T, hd), device=dev, generator=g).to(torch.bfloat16) for _ in range(2))
     scale = hd ** -0.5
     O, lse = attn_forward_inputs(torch, Q, K, V, scale)
     ws = torch.empty(sbp.attn_workspace_bytes(H, T, hd, chunk), dtype=torch.uint8, device=dev)
     dQ = torch.empty_like(Q)
-    dK = torch.empty((H, T, hd), dtype=torch.float32, device=dev)
-    dV = torch.empty((H, T, hd), dtype=torch.float32, device=dev)
+    dK = torch.empty((Hkv, T, hd), dtype=torch.float32, device=dev)
+    dV = torch.empty((Hkv, T, hd), dtype=torch.float32, device=dev)
     st = torch.zeros((), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -600,12 +603,13 @@ def run_attn_bench(args):
     else:
         names, gemms = ("k_attn (P, dS)", "k_bwd (dQ + dK, dV)"), (2, 3)
     line = {
-        "metric": ATTN_METRIC if (H, T, hd) == (32, 8192, 128) else f"attention bwd tokens/s (causal, H={H}, hd={hd}, T={T})",
+        "metric": ATTN_METRIC if (H, Hkv, T, hd) == (32, 32, 8192, 128) else
+        f"attention bwd tokens/s (causal, H={H}, Hkv={Hkv}, hd={hd}, T={T})",
         "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"causal_attn_bwd_bf16_H{H}_T{T}_hd{hd}_chunk{chunk}", "H": H, "T": T, "hd": hd,
-                   "chunk": chunk},
+        "config": {"workload": f"causal_attn_bwd_bf16_H{H}" + (f"_Hkv{Hkv}" if Hkv != H else "") +
+                   f"_T{T}_hd{hd}_chunk{chunk}", "H": H, "Hkv": Hkv, "T": T, "hd": hd, "chunk": chunk},
         "executed_tflops": flops * args.steps / (ms / 1000.0) / 1e12,
         "pct_bf16_peak": 100.0 * flops * args.steps / (ms / 1000.0) / 1e12 / peaks["bf16_tflops"],
         "chunk_buffer_gbs": pds_bytes * args.steps / (ms / 1000.0) / 1e9 if pds_bytes else None,
@@ -646,6 +650,8 @@ def main(argv=None):
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
     ap.add_argument("--hd", type=int, default=None, help="override the attention head width (--sublayer attn)")
+    ap.add_argument("--kv-heads", type=int, default=None,
+                    help="--sublayer attn: key / value heads (grouped-query attention; default = query heads)")
     ap.add_argument("--lean", action="store_true",
                     help="LM head: the smallest workspace (one chunk buffer, gradient as its own pass)")
     ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")

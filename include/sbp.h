@@ -219,6 +219,19 @@ int sbp_attn_causal_backward(const void* Q, const void* K, const void* V, const 
                              void* dQ, float* dK, float* dV, int accumulate,
                              void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* The same with grouped-query attention, as in the Qwen3 models of the pages'
+ * experiments: H query heads share Hkv key / value heads (H a multiple of Hkv); query
+ * head h reads key / value head h / (H / Hkv), and dK, dV of a key / value head sum over
+ * the query heads of its group.
+ *   Q, O, dO [H, T, hd] bf16; K, V [Hkv, T, hd] bf16; lse [H, T] fp32; dQ [H, T, hd] bf16;
+ *   dK, dV [Hkv, T, hd] fp32.
+ * Hkv = H is sbp_attn_causal_backward.  Hkv < H needs hd = 128 (SBP_ERR_UNSUPPORTED
+ * otherwise).  Workspace: sbp_attn_workspace_bytes(H, T, hd, chunk). */
+int sbp_attn_causal_backward_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                 const float* lse, int64_t H, int64_t Hkv, int64_t T, int64_t hd, float scale,
+                                 int64_t chunk, void* dQ, float* dK, float* dV, int accumulate,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Size of the fixed scratch array that sbp_lmhead_sft_noalloc works in (bytes). */
 #define SBP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

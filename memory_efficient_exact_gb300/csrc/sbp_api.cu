@@ -881,22 +881,22 @@ bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L)
 
 // hd = 128: per chunk, k_attn_kv (dK, dV of keys [0, c1)) then k_attn_q (dQ of the chunk)
 int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
-                   int64_t H, int64_t T, float scale, const AttnLayout& L, void* dQ, float* dK, float* dV,
-                   int accumulate, char* w, int32_t* dev_status, cudaStream_t s) {
+                   int64_t H, int64_t Hkv, int64_t T, float scale, const AttnLayout& L, void* dQ, float* dK,
+                   float* dV, int accumulate, char* w, int32_t* dev_status, cudaStream_t s) {
   const int64_t hd = 128;
   float* D = reinterpret_cast<float*>(w + L.off_d);
   int launches = 0;
   SBP_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
   if (!accumulate) {
-    SBP_CUDA(cudaMemsetAsync(dK, 0, (size_t)H * T * hd * sizeof(float), s));
-    SBP_CUDA(cudaMemsetAsync(dV, 0, (size_t)H * T * hd * sizeof(float), s));
+    SBP_CUDA(cudaMemsetAsync(dK, 0, (size_t)Hkv * T * hd * sizeof(float), s));
+    SBP_CUDA(cudaMemsetAsync(dV, 0, (size_t)Hkv * T * hd * sizeof(float), s));
   }
   if (T == 0) {
     g_launches = 0;
     return SBP_OK;
   }
   AttnFusedPlan plan;
-  if (!plan.init(Q, K, Vv, dO, dK, dV, T, H)) return SBP_ERR_CUDA;
+  if (!plan.init(Q, K, Vv, dO, dK, dV, T, H, Hkv)) return SBP_ERR_CUDA;
   {
     prof::Scope ps(3, s);
     k_attn_D<<<(unsigned)((H * T + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(O),
@@ -922,10 +922,12 @@ int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, 
 }
 
 int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
-             int64_t H, int64_t T, int64_t hd, float scale, int64_t chunk, void* dQ, float* dK, float* dV,
-             int accumulate, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s) {
+             int64_t H, int64_t Hkv, int64_t T, int64_t hd, float scale, int64_t chunk, void* dQ, float* dK,
+             float* dV, int accumulate, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s) {
   AttnLayout L;
   if (!attn_layout(H, T, hd, chunk, &L)) return SBP_ERR_INVALID_ARG;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return SBP_ERR_INVALID_ARG;
+  if (Hkv != H && !L.fused) return SBP_ERR_UNSUPPORTED;   // grouped heads: head dimension 128 only
   if (!dev_status || !dK || !dV) return SBP_ERR_INVALID_ARG;
   if (T > 0 && (!Q || !K || !Vv || !O || !dO || !lse || !dQ)) return SBP_ERR_INVALID_ARG;
   if (H * T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
@@ -933,7 +935,8 @@ int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const 
     if (q && !al16(q)) return SBP_ERR_ALIGNMENT;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return SBP_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
-  if (L.fused) return run_attn_fused(Q, K, Vv, O, dO, lse, H, T, scale, L, dQ, dK, dV, accumulate, w, dev_status, s);
+  if (L.fused)
+    return run_attn_fused(Q, K, Vv, O, dO, lse, H, Hkv, T, scale, L, dQ, dK, dV, accumulate, w, dev_status, s);
   void* pbuf = w + L.off_p;
   void* dsbuf = w + L.off_ds;
   float* D = reinterpret_cast<float*>(w + L.off_d);
@@ -1164,7 +1167,15 @@ int sbp_attn_causal_backward(const void* Q, const void* K, const void* V, const 
                              const float* lse, int64_t H, int64_t T, int64_t hd, float scale, int64_t chunk,
                              void* dQ, float* dK, float* dV, int accumulate, void* workspace, size_t ws_bytes,
                              int32_t* dev_status, void* stream) {
-  return run_attn(Q, K, V, O, dO, lse, H, T, hd, scale, chunk, dQ, dK, dV, accumulate, workspace, ws_bytes,
+  return run_attn(Q, K, V, O, dO, lse, H, H, T, hd, scale, chunk, dQ, dK, dV, accumulate, workspace, ws_bytes,
+                  dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int sbp_attn_causal_backward_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                 const float* lse, int64_t H, int64_t Hkv, int64_t T, int64_t hd, float scale,
+                                 int64_t chunk, void* dQ, float* dK, float* dV, int accumulate, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return run_attn(Q, K, V, O, dO, lse, H, Hkv, T, hd, scale, chunk, dQ, dK, dV, accumulate, workspace, ws_bytes,
                   dev_status, static_cast<cudaStream_t>(stream));
 }
 

@@ -243,6 +243,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 struct KvP {
   int H, T, c0, c1, nb, n_units;
+  int Hkv, group;    // key / value heads; query heads per key / value head (H = Hkv * group)
   float scale;
   const float* lse;  // [H, T]
   const float* D;    // [H, T]
@@ -250,14 +251,23 @@ struct KvP {
   uint64_t limit_ns;
 };
 
-// Unit u: head z, keys [256 kp, 256 kp + 256); query blocks b0 .. nb-1 of the chunk hold
-// at least one query at or after the unit's first key.  Key pairs in ascending order, so
-// the longest units start first.
-__device__ __forceinline__ void kv_unit(const KvP& p, int u, int& z, int& kp, int& b0) {
-  kp = u / p.H;
-  z = u - kp * p.H;
+// Unit u: key / value head zk, keys [256 kp, 256 kp + 256); query blocks b0 .. nb-1 of the
+// chunk hold at least one query at or after the unit's first key.  The unit walks those
+// blocks for each query head of zk's group (nblk blocks in all), accumulating dV and dK
+// of the shared head.  Key pairs in ascending order, so the longest units start first.
+__device__ __forceinline__ void kv_unit(const KvP& p, int u, int& zk, int& kp, int& b0, int& nblk) {
+  kp = u / p.Hkv;
+  zk = u - kp * p.Hkv;
   const int num = 256 * kp - p.c0 - 127;
   b0 = num <= 0 ? 0 : (num + 127) / 128;
+  nblk = p.group * (p.nb - b0);
+}
+// Block n of a unit: query head z of the group, query block b of the chunk.
+__device__ __forceinline__ void kv_block(const KvP& p, int zk, int b0, int n, int& z, int& b) {
+  const int nbl = p.nb - b0;
+  const int gh = n / nbl;
+  z = zk * p.group + gh;
+  b = b0 + (n - gh * nbl);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
@@ -286,21 +296,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       uint32_t pha = 0, phr = 0, iss = 0, lph_a[2] = {0, 0}, lph_r = 0;
       bool ok = true;
       for (int u = pid; u < p.n_units && ok; u += npairs) {
-        int z, kp, b0;
-        kv_unit(p, u, z, kp, b0);
+        int zk, kp, b0, nblk;
+        kv_unit(p, u, zk, kp, b0, nblk);
         if (!wait_bounded(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
         const uint32_t fr = mapa(saddr(&c->rfull), 0);
         if (rank == 0) mbar_expect_tx(&c->rfull, 4u * 32768u);
         const int krow = 256 * kp + 128 * (int)rank;
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
-          tma_load_3d_pair(sb + KV_K + hb * 16384, &tmK, fr, 64 * hb, krow, z);
-          tma_load_3d_pair(sb + KV_V + hb * 16384, &tmV, fr, 64 * hb, krow, z);
+          tma_load_3d_pair(sb + KV_K + hb * 16384, &tmK, fr, 64 * hb, krow, zk);
+          tma_load_3d_pair(sb + KV_V + hb * 16384, &tmV, fr, 64 * hb, krow, zk);
         }
         iss |= 4u;
         lph_r = phr;
         phr ^= 1u;
-        for (int b = b0; b < p.nb; ++b) {
+        for (int n = 0; n < nblk; ++n) {
+          int z, b;
+          kv_block(p, zk, b0, n, z, b);
           if (!wait_bounded(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fa = mapa(saddr(&c->afull[sa]), 0);
           if (rank == 0) mbar_expect_tx(&c->afull[sa], 2u * KV_A_STAGE);
@@ -331,9 +343,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       uint32_t phb = 0, lph = 0;
       bool ok = true, any = false;
       for (int u = pid; u < p.n_units && ok; u += npairs) {
-        int z, kp, b0;
-        kv_unit(p, u, z, kp, b0);
-        for (int b = b0; b < p.nb; ++b) {
+        int zk, kp, b0, nblk;
+        kv_unit(p, u, zk, kp, b0, nblk);
+        for (int n = 0; n < nblk; ++n) {
+          int z, b;
+          kv_block(p, zk, b0, n, z, b);
           if (!wait_bounded(&c->bempty[0], phb ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fb = mapa(saddr(&c->bfull[0]), 0);
           if (rank == 0) mbar_expect_tx(&c->bfull[0], 4u * 16384u);
@@ -378,9 +392,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         return true;
       };
       for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
-        int z, kp, b0;
-        kv_unit(p, u, z, kp, b0);
-        const int nbl = p.nb - b0;
+        int zk, kp, b0, nbl;
+        kv_unit(p, u, zk, kp, b0, nbl);
         if (!wait_bounded(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
         phr ^= 1u;
         tc_fence_after();
@@ -418,9 +431,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       uint32_t te_seen = 0, or_seen = 0, g = 0;
       bool ok = true;
       for (int u = pid; u < p.n_units && ok; u += npairs) {
-        int z, kp, b0;
-        kv_unit(p, u, z, kp, b0);
-        for (int b = b0; b < p.nb; ++b, ++g)
+        int zk, kp, b0, nblk;
+        kv_unit(p, u, zk, kp, b0, nblk);
+        for (int n = 0; n < nblk; ++n, ++g)
           if (!forward_block(c, g, te_seen, or_seen, p.limit_ns)) { ok = false; break; }
       }
       if (!ok) fail_f(c, p.status);
@@ -432,10 +445,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
     float* ld = reinterpret_cast<float*>(base + KV_LD);
     uint32_t lempty_seen = 0, g = 0;
     for (int u = pid; u < p.n_units; u += npairs) {
-      int z, kp, b0;
-      kv_unit(p, u, z, kp, b0);
+      int zk, kp, b0, nblk;
+      kv_unit(p, u, zk, kp, b0, nblk);
       bool ok = true;
-      for (int b = b0; b < p.nb; ++b, ++g) {
+      for (int n = 0; n < nblk; ++n, ++g) {
+        int z, b;
+        kv_block(p, zk, b0, n, z, b);
         float lv[4], dv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -469,11 +484,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
     int lu = 0;
     bool ok = true;
     for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
-      int z, kp, b0;
-      kv_unit(p, u, z, kp, b0);
+      int zk, kp, b0, nblk;
+      kv_unit(p, u, zk, kp, b0, nblk);
       const int kw = 256 * kp + 128 * (int)rank + 32 * q;   // this warp's first key
       const int key = kw + lane;
-      for (int b = b0; b < p.nb; ++b, ++g) {
+      for (int n = 0; n < nblk; ++n, ++g) {
+        int z, b;
+        kv_block(p, zk, b0, n, z, b);
+        (void)z;
         if (!warp_wait_n(&c->tfull, tfull_seen, g + 1, c, p.limit_ns) ||
             !warp_wait_n(&c->lfull, lfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
@@ -528,7 +546,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         // the previous block's accumulation has read P^T and dS^T; at a unit's first
         // block, also the previous unit's dV / dK staging has left this area
         if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns) ||
-            (b == b0 && !warp_wait_n(&c->sfree, sfree_seen, (uint32_t)lu, c, p.limit_ns))) { ok = false; break; }
+            (n == 0 && !warp_wait_n(&c->sfree, sfree_seen, (uint32_t)lu, c, p.limit_ns))) { ok = false; break; }
         store_half_row(sb + KV_PT + (cg >> 1) * 16384, lrow, cg & 1, pw);
         store_half_row(sb + KV_DST + (cg >> 1) * 16384, lrow, cg & 1, dw);
         fence_proxy_async();
@@ -567,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(t ? &tmdK : &tmdV, stg, 32 * cg, kw, z);
+          tma_reduce_add_3d(t ? &tmdK : &tmdV, stg, 32 * cg, kw, zk);
           bulk_commit();
         }
       }
@@ -586,6 +604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
 
 struct QP {
   int H, T, c0, c1, n_qp, n_units;
+  int group;         // query heads per key / value head
   float scale;
   const float* lse;
   const float* D;
@@ -651,8 +670,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
           const int krow = 128 * j + 64 * (int)rank;
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
-            tma_load_3d_pair(st + hb * 8192, &tmKa, fa, 64 * hb, krow, z);
-            tma_load_3d_pair(st + 16384 + hb * 8192, &tmVa, fa, 64 * hb, krow, z);
+            tma_load_3d_pair(st + hb * 8192, &tmKa, fa, 64 * hb, krow, z / p.group);
+            tma_load_3d_pair(st + 16384 + hb * 8192, &tmVa, fa, 64 * hb, krow, z / p.group);
           }
           iss |= 1u << sa;
           lph_a[sa] = pha;
@@ -680,7 +699,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
           if (!wait_bounded(&c->bempty[sy], phy ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fb = mapa(saddr(&c->bfull[sy]), 0);
           if (rank == 0) mbar_expect_tx(&c->bfull[sy], 2u * Q_Y_STAGE);
-          tma_load_3d_pair(sb + Q_Y + sy * Q_Y_STAGE, &tmKb, fb, 64 * (int)rank, 128 * j, z);
+          tma_load_3d_pair(sb + Q_Y + sy * Q_Y_STAGE, &tmKb, fb, 64 * (int)rank, 128 * j, z / p.group);
           iss |= 1u << sy;
           lph[sy] = phy;
           if (++sy == 2) { sy = 0; phy ^= 1u; }
@@ -904,13 +923,15 @@ bool fused_attrs() {
 }  // namespace
 
 bool AttnFusedPlan::init(const void* Q, const void* K, const void* V, const void* dO, float* dK_, float* dV_,
-                         int64_t T_, int64_t H_) {
+                         int64_t T_, int64_t H_, int64_t Hkv_) {
   T = T_;
   H = H_;
-  return map3_bf16(&K128, K, T, H, 128) && map3_bf16(&V128, V, T, H, 128) && map3_bf16(&Q64, Q, T, H, 64) &&
+  Hkv = Hkv_;
+  // query-side operands over H heads, key / value side (and dK, dV) over Hkv heads
+  return map3_bf16(&K128, K, T, Hkv, 128) && map3_bf16(&V128, V, T, Hkv, 128) && map3_bf16(&Q64, Q, T, H, 64) &&
          map3_bf16(&O64, dO, T, H, 64) && map3_bf16(&Q128, Q, T, H, 128) && map3_bf16(&O128, dO, T, H, 128) &&
-         map3_bf16(&K64, K, T, H, 64) && map3_bf16(&V64, V, T, H, 64) && map3_f32(&dK, dK_, T, H) &&
-         map3_f32(&dV, dV_, T, H);
+         map3_bf16(&K64, K, T, Hkv, 64) && map3_bf16(&V64, V, T, Hkv, 64) && map3_f32(&dK, dK_, T, Hkv) &&
+         map3_f32(&dV, dV_, T, Hkv);
 }
 
 cudaError_t attn_fused_kv(const AttnFusedPlan& plan, int64_t c0, int64_t c1, float scale, const float* lse,
@@ -921,7 +942,9 @@ cudaError_t attn_fused_kv(const AttnFusedPlan& plan, int64_t c0, int64_t c1, flo
   KvP p;
   p.H = (int)plan.H; p.T = (int)plan.T; p.c0 = (int)c0; p.c1 = (int)c1;
   p.nb = (int)((c1 - c0 + 127) / 128);
-  p.n_units = (int)((c1 + 255) / 256) * p.H;
+  p.Hkv = (int)plan.Hkv;
+  p.group = (int)(plan.H / plan.Hkv);
+  p.n_units = (int)((c1 + 255) / 256) * p.Hkv;
   p.scale = scale; p.lse = lse; p.D = D; p.status = status; p.limit_ns = wait_limit_ns();
   int pairs = max_pairs((const void*)k_attn_kv, SMEM_KV, KV_THREADS);
   if (pairs > p.n_units) pairs = p.n_units;
@@ -939,6 +962,7 @@ cudaError_t attn_fused_q(const AttnFusedPlan& plan, int64_t c0, int64_t c1, floa
   p.H = (int)plan.H; p.T = (int)plan.T; p.c0 = (int)c0; p.c1 = (int)c1;
   p.n_qp = (int)((c1 - c0 + 255) / 256);
   p.n_units = p.n_qp * p.H;
+  p.group = (int)(plan.H / plan.Hkv);
   p.scale = scale; p.lse = lse; p.D = D; p.dQ = static_cast<__nv_bfloat16*>(dQ);
   p.status = status; p.limit_ns = wait_limit_ns();
   int pairs = max_pairs((const void*)k_attn_q, SMEM_Q, Q_THREADS);

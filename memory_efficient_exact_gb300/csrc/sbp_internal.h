@@ -108,10 +108,10 @@ cudaError_t tc_attn(const TcAttnArgs& a, bool ds, cudaStream_t s);
 // and k_attn_q writes dQ of the chunk's rows (bf16); P and dS never leave the chip.
 // The tensor maps are built once per call (init) and serve every chunk.
 struct AttnFusedPlan {
-  int64_t T = 0, H = 0;
+  int64_t T = 0, H = 0, Hkv = 0;   // query heads H = Hkv x group (grouped-query attention)
   CUtensorMap K128, V128, Q64, O64, Q128, O128, K64, V64, dK, dV;
   bool init(const void* Q, const void* K, const void* V, const void* dO, float* dK, float* dV, int64_t T,
-            int64_t H);
+            int64_t H, int64_t Hkv);
 };
 cudaError_t attn_fused_kv(const AttnFusedPlan& plan, int64_t c0, int64_t c1, float scale, const float* lse,
                           const float* D, int32_t* status, cudaStream_t s);

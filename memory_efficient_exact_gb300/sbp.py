@@ -65,6 +65,9 @@ def _load() -> ctypes.CDLL:
     lib.sbp_attn_workspace_bytes.argtypes = [I64, I64, I64, I64]
     lib.sbp_attn_causal_backward.restype = C
     lib.sbp_attn_causal_backward.argtypes = [P, P, P, P, P, P, I64, I64, I64, F, I64, P, P, P, C, P, SZ, P, P]
+    lib.sbp_attn_causal_backward_gqa.restype = C
+    lib.sbp_attn_causal_backward_gqa.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, F, I64, P, P, P, C, P, SZ, P,
+                                                 P]
     lib.sbp_status_string.restype = ctypes.c_char_p
     lib.sbp_status_string.argtypes = [C]
     lib.sbp_last_launch_count.restype = C
@@ -347,14 +350,21 @@ def attn_workspace_bytes(H: int, T: int, hd: int, chunk: int) -> int:
 
 def attn_causal_backward(Q, K, V, O, dO, lse, scale, chunk, *, dQ=None, dK=None, dV=None, accumulate=False,
                          workspace=None, status=None, stream=None) -> dict:
-    """Chunked causal-attention backward (``sbp_attn_causal_backward``).
+    """Chunked causal-attention backward (``sbp_attn_causal_backward``, or
+    ``sbp_attn_causal_backward_gqa`` when K and V have fewer heads than Q).
 
-    Q, K, V, O, dO [H, T, hd] bf16; lse [H, T] fp32 (the forward's row log-sum-exp)."""
+    Q, O, dO [H, T, hd] bf16; K, V [Hkv, T, hd] bf16 (Hkv divides H; Hkv = H is plain
+    multi-head attention); lse [H, T] fp32 (the forward's row log-sum-exp).  dK, dV are
+    [Hkv, T, hd] fp32."""
     _dev(Q, K, V, O, dO, lse)
     H, T, hd = Q.shape
-    for t in (K, V, O, dO):
+    Hkv = K.shape[0]
+    for t in (O, dO):
         if t.shape != (H, T, hd) or t.dtype != torch.bfloat16:
-            raise ValueError("Q, K, V, O, dO must be bf16 [H, T, hd]")
+            raise ValueError("Q, O, dO must be bf16 [H, T, hd]")
+    for t in (K, V):
+        if t.shape != (Hkv, T, hd) or t.dtype != torch.bfloat16:
+            raise ValueError("K, V must be bf16 [Hkv, T, hd]")
     if Q.dtype != torch.bfloat16 or lse.shape != (H, T) or lse.dtype != torch.float32:
         raise ValueError("Q bf16 [H, T, hd]; lse fp32 [H, T]")
     dev = Q.device
@@ -364,11 +374,17 @@ def attn_causal_backward(Q, K, V, O, dO, lse, scale, chunk, *, dQ=None, dK=None,
             raise SbpError(ERR_INVALID_ARG, "attn_workspace_bytes")
         workspace = torch.empty(n, dtype=torch.uint8, device=dev)
     dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty((H, T, hd), dtype=torch.float32, device=dev) if dK is None else dK
-    dV = torch.empty((H, T, hd), dtype=torch.float32, device=dev) if dV is None else dV
+    dK = torch.empty((Hkv, T, hd), dtype=torch.float32, device=dev) if dK is None else dK
+    dV = torch.empty((Hkv, T, hd), dtype=torch.float32, device=dev) if dV is None else dV
     _dev(dQ, dK, dV)
     st = torch.empty((), dtype=torch.int32, device=dev) if status is None else status
-    _check(_lib.sbp_attn_causal_backward(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(lse), H, T, hd, float(scale), chunk,
-                                         _p(dQ), _p(dK), _p(dV), int(bool(accumulate)), _p(workspace),
-                                         workspace.numel(), _p(st), _stream(stream)), "sbp_attn_causal_backward")
+    if Hkv == H:
+        _check(_lib.sbp_attn_causal_backward(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(lse), H, T, hd, float(scale),
+                                             chunk, _p(dQ), _p(dK), _p(dV), int(bool(accumulate)), _p(workspace),
+                                             workspace.numel(), _p(st), _stream(stream)), "sbp_attn_causal_backward")
+    else:
+        _check(_lib.sbp_attn_causal_backward_gqa(_p(Q), _p(K), _p(V), _p(O), _p(dO), _p(lse), H, Hkv, T, hd,
+                                                 float(scale), chunk, _p(dQ), _p(dK), _p(dV), int(bool(accumulate)),
+                                                 _p(workspace), workspace.numel(), _p(st), _stream(stream)),
+               "sbp_attn_causal_backward_gqa")
     return dict(dQ=dQ, dK=dK, dV=dV, status=st)

@@ -28,9 +28,11 @@ def sbp():
     return mod
 
 
-def make(H, T, hd, seed):
+def make(H, T, hd, seed, Hkv=None):
     g = np.random.default_rng(seed)
-    Q, K, V, dO = (I.round_bf16(g.standard_normal((H, T, hd), dtype=np.float32)) for _ in range(4))
+    Hkv = H if Hkv is None else Hkv
+    Q, dO = (I.round_bf16(g.standard_normal((H, T, hd), dtype=np.float32)) for _ in range(2))
+    K, V = (I.round_bf16(g.standard_normal((Hkv, T, hd), dtype=np.float32)) for _ in range(2))
     scale = 1.0 / np.sqrt(hd)
     f = A.forward(Q, K, V, scale)
     O = I.round_bf16(f["O"].astype(np.float32))
@@ -62,6 +64,31 @@ def test_attention_backward_parity(sbp, H, T, hd, chunk):
     assert max(e.values()) <= 2e-2, e
 
 
+# grouped-query attention (key / value heads shared by H / Hkv query heads, the Qwen3
+# layout): head dimension 128, groups of 2, 3 and 4, one shared head (multi-query), ragged
+# chunks, and more units than SM pairs
+@pytest.mark.parametrize("H,Hkv,T,chunk", [(8, 2, 640, 256), (4, 1, 513, 200), (6, 3, 96, 40),
+                                           (48, 8, 1024, 512), (2, 1, 1, 1)])
+def test_attention_gqa_parity(sbp, H, Hkv, T, chunk):
+    hd = 128
+    Q, K, V, O, dO, lse, scale = make(H, T, hd, seed=H * 100 + Hkv * 10 + T, Hkv=Hkv)
+    out = sbp.attn_causal_backward(dev(Q), dev(K), dev(V), dev(O), dev(dO), dev(lse, torch.float32), scale, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    assert out["dK"].shape == (Hkv, T, hd) and out["dV"].shape == (Hkv, T, hd)
+    ref = A.backward(Q, K, V, O, dO, lse, scale)
+    e = {"dQ": rel_fro(out["dQ"].float().cpu().numpy(), ref["dQ"]),
+         "dK": rel_fro(out["dK"].cpu().numpy(), ref["dK"]),
+         "dV": rel_fro(out["dV"].cpu().numpy(), ref["dV"])}
+    assert max(e.values()) <= 2e-2, e
+
+
+def test_attention_gqa_needs_hd128(sbp):
+    Q, K, V, O, dO, lse, scale = make(4, 64, 64, seed=3, Hkv=2)
+    with pytest.raises(sbp.SbpError):
+        sbp.attn_causal_backward(dev(Q), dev(K), dev(V), dev(O), dev(dO), dev(lse, torch.float32), scale, 32)
+
+
 @pytest.mark.parametrize("hd", [64, 128])
 def test_attention_accumulate_and_determinism(sbp, hd):
     H, T, chunk = 2, 300, 128
@@ -78,31 +105,39 @@ def test_attention_accumulate_and_determinism(sbp, hd):
         assert torch.allclose(acc, 2 * ref, rtol=1e-5, atol=1e-6 * ref.abs().max().item())
 
 
-def test_attention_fullsize_sampled(sbp):
-    """The benchmark's workload and launch configuration (H=32, T=8192, hd=128, chunk
-    1024): dQ on sampled query rows and dK, dV on sampled keys of two heads against the
-    oracle's row and column forms (chunk starts and ends, the first and last token,
-    random picks).  The two heads' O and lse come from the oracle's forward; the other
-    heads' from a plain fp32 torch forward (they only have to be valid inputs)."""
+@pytest.mark.parametrize("Hkv", [32, 8])
+def test_attention_fullsize_sampled(sbp, Hkv):
+    """The benchmark's workload and launch configuration (H=32 query heads, T=8192,
+    hd=128, chunk 1024), with 32 key / value heads (multi-head) and with 8 (grouped, the
+    Qwen3-8B layout): dQ on sampled query rows and dK, dV on sampled keys of the first and
+    last key / value heads against the oracle's row and column forms (chunk starts and
+    ends, the first and last token, random picks).  The O and lse of every query head in
+    those heads' groups come from the oracle's forward; the other heads' from a plain
+    fp32 torch forward (they only have to be valid inputs)."""
     H, T, hd, chunk = 32, 8192, 128, 1024
-    g = np.random.default_rng(81920)
-    Q, K, V, dO = (I.round_bf16(g.standard_normal((H, T, hd), dtype=np.float32)) for _ in range(4))
+    g = np.random.default_rng(81920 + Hkv)
+    Q, dO = (I.round_bf16(g.standard_normal((H, T, hd), dtype=np.float32)) for _ in range(2))
+    K, V = (I.round_bf16(g.standard_normal((Hkv, T, hd), dtype=np.float32)) for _ in range(2))
+    grp = H // Hkv
     scale = 1.0 / np.sqrt(hd)
     tq, tk, tv, tdo = dev(Q), dev(K), dev(V), dev(dO)
     O = torch.empty_like(tq)
     lse = torch.empty((H, T), dtype=torch.float32, device="cuda")
     mask = torch.ones((T, T), dtype=torch.bool, device="cuda").triu(1)
     for h in range(H):
-        S = (tq[h].float() @ tk[h].float().T) * scale
+        S = (tq[h].float() @ tk[h // grp].float().T) * scale
         S.masked_fill_(mask, float("-inf"))
         lse[h] = torch.logsumexp(S, dim=1)
-        O[h] = (torch.exp(S - lse[h][:, None]) @ tv[h].float()).to(torch.bfloat16)
+        O[h] = (torch.exp(S - lse[h][:, None]) @ tv[h // grp].float()).to(torch.bfloat16)
     del S, mask
-    heads = (0, H - 1)
+    # query heads whose rows are checked, and the key / value heads whose dK, dV are: all
+    # query heads of a checked key / value head's group need oracle O and lse
+    kv_heads = (0, Hkv - 1)
+    heads = sorted({h for hk in kv_heads for h in range(hk * grp, (hk + 1) * grp)})
     On = O.float().cpu().numpy()
     lsen = lse.cpu().numpy()
     for h in heads:
-        f = A.forward(Q[h:h + 1], K[h:h + 1], V[h:h + 1], scale)
+        f = A.forward(Q[h:h + 1], K[h // grp:h // grp + 1], V[h // grp:h // grp + 1], scale)
         On[h] = I.round_bf16(f["O"][0].astype(np.float32))
         lsen[h] = f["lse"][0].astype(np.float32)
         O[h] = dev(On[h])
@@ -113,9 +148,12 @@ def test_attention_fullsize_sampled(sbp):
     edges = [0, 1, 127, 128, 255, 256, 1023, 1024, 1025, 4095, 4096, 7167, 7168, 8190, 8191]
     rows = sorted(set(edges) | set(g.integers(0, T, 20).tolist()))
     keys = sorted(set(edges) | set(g.integers(0, T, 20).tolist()))
-    dQ, dK, dV = (out[k][list(heads)].float().cpu().numpy() for k in ("dQ", "dK", "dV"))
-    for i, h in enumerate(heads):
+    dQ = out["dQ"].float().cpu().numpy()
+    dK, dV = out["dK"].cpu().numpy(), out["dV"].cpu().numpy()
+    for h in (heads[0], heads[-1]):
         rq = A.rows_dQ(Q, K, V, On, dO, lsen, scale, h, rows)
-        rk, rv = A.keys_dKdV(Q, K, V, On, dO, lsen, scale, h, keys)
-        e = {"dQ": rel_fro(dQ[i][rows], rq), "dK": rel_fro(dK[i][keys], rk), "dV": rel_fro(dV[i][keys], rv)}
-        assert max(e.values()) <= 2e-2, (h, e)
+        assert rel_fro(dQ[h][rows], rq) <= 2e-2, (h, rel_fro(dQ[h][rows], rq))
+    for hk in kv_heads:
+        rk, rv = A.keys_dKdV(Q, K, V, On, dO, lsen, scale, hk, keys)
+        e = {"dK": rel_fro(dK[hk][keys], rk), "dV": rel_fro(dV[hk][keys], rv)}
+        assert max(e.values()) <= 2e-2, (hk, e)
