@@ -879,7 +879,43 @@ bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L)
   return true;
 }
 
-// hd = 128: per chunk, k_attn_kv (dK, dV of keys [0, c1)) then k_attn_q (dQ of the chunk)
+// A second stream per device, for the work of one call that may run beside the caller's
+// stream: forked from it after an event and joined back into it before the call returns,
+// so the caller sees one ordered call on its own stream.  The lock is held while a call
+// enqueues its fork .. join, so concurrent calls never mix their events.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+static SideStream g_side[64];
+static std::mutex g_side_init;
+
+SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_side_init);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    ss.s = st;
+    ss.fork = a;
+    ss.join = b;
+  }
+  return &ss;
+}
+
+// hd = 128: per chunk, k_attn_kv (dK, dV of keys [0, c1)) on the caller's stream and
+// k_attn_q (dQ of the chunk) on the side stream: the two families write disjoint outputs,
+// so they may overlap (each fills the other's last, partly occupied wave); each family
+// stays in chunk order on its own stream, so the results do not depend on the overlap
 int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
                    int64_t H, int64_t Hkv, int64_t T, float scale, const AttnLayout& L, void* dQ, float* dK,
                    float* dV, int accumulate, char* w, int32_t* dev_status, cudaStream_t s) {
@@ -904,19 +940,35 @@ int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, 
     ++launches;
     SBP_CUDA(cudaGetLastError());
   }
-  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+  SideStream* ss = side_stream();
+  std::unique_lock<std::mutex> lk;
+  cudaStream_t sq = s;
+  if (ss) {
+    lk = std::unique_lock<std::mutex>(ss->mu);
+    SBP_CUDA(cudaEventRecord(ss->fork, s));
+    SBP_CUDA(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+    sq = ss->s;
+  }
+  int rc = SBP_OK;
+  for (int64_t ci = 0; ci < L.n_chunks && rc == SBP_OK; ++ci) {
     const int64_t c0 = ci * L.chunk, c1 = std::min(T, c0 + L.chunk);
     {
       prof::Scope ps(0, s);
-      SBP_CUDA(attn_fused_kv(plan, c0, c1, scale, lse, D, dev_status, s));
+      if (attn_fused_kv(plan, c0, c1, scale, lse, D, dev_status, s) != cudaSuccess) rc = SBP_ERR_CUDA;
       ++launches;
     }
+    if (rc != SBP_OK) break;
     {
-      prof::Scope ps(1, s);
-      SBP_CUDA(attn_fused_q(plan, c0, c1, scale, lse, D, dQ, dev_status, s));
+      prof::Scope ps(1, sq);
+      if (attn_fused_q(plan, c0, c1, scale, lse, D, dQ, dev_status, sq) != cudaSuccess) rc = SBP_ERR_CUDA;
       ++launches;
     }
   }
+  if (ss) {   // join even after an error, so the caller's stream is never left behind
+    if (cudaEventRecord(ss->join, sq) != cudaSuccess || cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess)
+      rc = SBP_ERR_CUDA;
+  }
+  if (rc != SBP_OK) return rc;
   g_launches = launches;
   return SBP_OK;
 }
