@@ -212,7 +212,10 @@ int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, cons
  *   log-sum-exp of s Q K^T per query row; dQ [H, T, hd] bf16 (overwritten);
  *   dK, dV [H, T, hd] fp32 (overwritten when accumulate = 0, added to when 1).
  * hd must be a multiple of 64, at most 256.  Workspace, stream and error rules as for the
- * LM-head calls. */
+ * LM-head calls; at hd = 128 the dQ kernels run on an internal stream of the library
+ * (one per device) that is forked from `stream` by an event after the call's first
+ * kernel and joined back into it by another before the call returns, so the work still
+ * completes in order on `stream` (and can be captured into a CUDA graph from `stream`). */
 size_t sbp_attn_workspace_bytes(int64_t H, int64_t T, int64_t hd, int64_t chunk);
 int sbp_attn_causal_backward(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                              const float* lse, int64_t H, int64_t T, int64_t hd, float scale, int64_t chunk,
