@@ -737,6 +737,39 @@ bool mlp_layout(int64_t T, int64_t d, int64_t f, int64_t chunk, MlpLayout* L) {
   return true;
 }
 
+// A second stream per device, for the work of one call that may run beside the caller's
+// stream: forked from it after an event and joined back into it before the call returns,
+// so the caller sees one ordered call on its own stream.  The lock is held while a call
+// enqueues its fork .. join, so concurrent calls never mix their events.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+static SideStream g_side[64];
+static std::mutex g_side_init;
+
+SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_side_init);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    ss.s = st;
+    ss.fork = a;
+    ss.join = b;
+  }
+  return &ss;
+}
+
 int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int64_t T, int64_t d, int64_t f,
             int64_t chunk, void* dX, float* dWgu, float* dWd, int accumulate, void* ws, size_t ws_bytes,
             int32_t* dev_status, cudaStream_t s) {
@@ -762,19 +795,36 @@ int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int6
     launches += 2;
     SBP_CUDA(cudaGetLastError());
   }
-  for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+  // dWd (+)= dY_c^T a_c needs only the chunk's a: it runs on the side stream beside the
+  // chunk's da and dX GEMMs (fork after a is formed, join before the next chunk overwrites
+  // a); the dWd launches stay in chunk order on that stream, so the sums keep their order
+  SideStream* ss = T > 0 ? side_stream() : nullptr;
+  std::unique_lock<std::mutex> lk;
+  if (ss) lk = std::unique_lock<std::mutex>(ss->mu);
+  cudaStream_t se = ss ? ss->s : s;
+  int rc = SBP_OK;
+#define MLP_CUDA(x)                                  \
+  do {                                               \
+    if ((x) != cudaSuccess) { rc = SBP_ERR_CUDA; break; } \
+  } while (0)
+  for (int64_t ci = 0; ci < L.n_chunks && rc == SBP_OK; ++ci) {
     const int64_t r0 = ci * L.chunk;
     const int rows = (int)((r0 + L.chunk <= T) ? L.chunk : T - r0);
     const int acc = (ci > 0 || accumulate) ? 1 : 0;
+    if (ss && ci > 0 && cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess) { rc = SBP_ERR_CUDA; break; }
     {
       // recompute g, u and a = silu(g) u for the chunk, then dg | du in place
       prof::Scope ps(0, s);
       TcMlpArgs m{};
       m.Arows = X; m.T = T; m.d = d; m.f = f; m.B = Wgu; m.r0 = r0; m.rows = rows; m.Aout = abuf; m.GU = gu;
       m.status = dev_status;
-      SBP_CUDA(tc_mlp(m, false, s));
+      if (tc_mlp(m, false, s) != cudaSuccess) { rc = SBP_ERR_CUDA; break; }
+      if (ss && (cudaEventRecord(ss->fork, s) != cudaSuccess || cudaStreamWaitEvent(se, ss->fork, 0) != cudaSuccess)) {
+        rc = SBP_ERR_CUDA;
+        break;
+      }
       m.Arows = dY; m.B = Wd;
-      SBP_CUDA(tc_mlp(m, true, s));
+      if (tc_mlp(m, true, s) != cudaSuccess) { rc = SBP_ERR_CUDA; break; }
       launches += 2;
     }
     const int splits = std::min(choose_splits(rows, d, 2 * f, num_sms()), L.splits);
@@ -785,14 +835,19 @@ int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int6
       b.G = gu; b.ldg = 2 * f; b.H = X; b.W = Wgu; b.T = T; b.d = d; b.V = 2 * f; b.r0 = r0; b.rows = rows;
       b.splits = splits; b.dh_part = dhp; b.dW = dWgu; b.dw_accumulate = acc; b.counter = cnt + 2 * ci;
       b.status = dev_status;
-      SBP_CUDA(tc_backward(b, s));
+      if (tc_backward(b, s) != cudaSuccess) { rc = SBP_ERR_CUDA; break; }
+      ++launches;
+    }
+    {
       // dWd (+)= dY_c^T a_c : the dW units only, with M over d and N over f
+      prof::Scope ps(1, se);
       TcBwdArgs e{};
       e.G = static_cast<const __nv_bfloat16*>(dY) + r0 * d; e.ldg = d; e.H = abuf; e.W = Wd; e.T = rows;
       e.d = f; e.V = d; e.r0 = 0; e.rows = rows; e.splits = 1; e.dh_part = dhp; e.dW = dWd;
       e.dw_accumulate = acc; e.counter = cnt + 2 * ci + 1; e.status = dev_status; e.dw_only = 1;
-      SBP_CUDA(tc_backward(e, s));
-      launches += 2;
+      if (tc_backward(e, se) != cudaSuccess) { rc = SBP_ERR_CUDA; break; }
+      if (ss && cudaEventRecord(ss->join, se) != cudaSuccess) { rc = SBP_ERR_CUDA; break; }
+      ++launches;
     }
     {
       prof::Scope ps(3, s);
@@ -800,9 +855,17 @@ int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int6
       k_dh_reduce<__nv_bfloat16><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
           dhp, splits, n, n, static_cast<__nv_bfloat16*>(dX) + r0 * d);
       ++launches;
-      SBP_CUDA(cudaGetLastError());
+      MLP_CUDA(cudaGetLastError());
     }
   }
+#undef MLP_CUDA
+  // join: the caller's stream waits for the last dWd (the side stream has waited on it for
+  // every fork, so nothing of this call is left behind even after an error)
+  if (ss && L.n_chunks > 0) {
+    if (cudaEventRecord(ss->join, se) != cudaSuccess || cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess)
+      rc = SBP_ERR_CUDA;
+  }
+  if (rc != SBP_OK) return rc;
   g_launches = launches;
   return SBP_OK;
 }
@@ -877,39 +940,6 @@ bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L)
   l.total = o;
   *L = l;
   return true;
-}
-
-// A second stream per device, for the work of one call that may run beside the caller's
-// stream: forked from it after an event and joined back into it before the call returns,
-// so the caller sees one ordered call on its own stream.  The lock is held while a call
-// enqueues its fork .. join, so concurrent calls never mix their events.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  std::mutex mu;
-};
-static SideStream g_side[64];
-static std::mutex g_side_init;
-
-SideStream* side_stream() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(g_side_init);
-  SideStream& ss = g_side[dev];
-  if (!ss.s) {
-    cudaStream_t st = nullptr;
-    cudaEvent_t a = nullptr, b = nullptr;
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    ss.s = st;
-    ss.fork = a;
-    ss.join = b;
-  }
-  return &ss;
 }
 
 // hd = 128: per chunk, k_attn_kv (dK, dV of keys [0, c1)) on the caller's stream and
