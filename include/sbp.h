@@ -191,7 +191,9 @@ int sbp_profile_read(double* ms, int64_t* launches, int n);
  *   Wd [d, f] bf16;  dX [T, d] bf16 (overwritten);  dWgu [2f, d] fp32, dWd [d, f] fp32
  *   (overwritten when accumulate = 0, added to when 1).
  * d must be a multiple of 64 and f of 256.  Workspace, stream and error rules as for the
- * LM-head calls. */
+ * LM-head calls; the dWd GEMMs run on an internal stream of the library (one per device)
+ * forked from `stream` and joined back into it by events within the call, so the work
+ * still completes in order on `stream`. */
 size_t sbp_mlp_workspace_bytes(int64_t T, int64_t d, int64_t f, int64_t chunk);
 int sbp_mlp_swiglu_backward(const void* X, const void* Wgu, const void* Wd, const void* dY,
                             int64_t T, int64_t d, int64_t f, int64_t chunk,
