@@ -157,3 +157,52 @@ def test_attention_fullsize_sampled(sbp, Hkv):
         rk, rv = A.keys_dKdV(Q, K, V, On, dO, lsen, scale, hk, keys)
         e = {"dK": rel_fro(dK[hk][keys], rk), "dV": rel_fro(dV[hk][keys], rv)}
         assert max(e.values()) <= 2e-2, (hk, e)
+
+
+def test_side_stream_under_graph_capture_and_threads(sbp):
+    """The hd = 128 path runs its dQ kernels on the library's side stream, forked from the
+    caller's stream and joined back into it: a call captured into a CUDA graph and
+    replayed, and calls from two host threads on two streams, give the same bits as a
+    plain call."""
+    import threading
+    H, T, hd, chunk = 4, 640, 128, 256
+    Q, K, V, O, dO, lse, scale = make(H, T, hd, seed=77)
+    args = [dev(Q), dev(K), dev(V), dev(O), dev(dO), dev(lse, torch.float32), scale, chunk]
+    ref = sbp.attn_causal_backward(*args)
+    torch.cuda.synchronize()
+    # graph capture on a side stream of the caller's
+    s = torch.cuda.Stream()
+    ws = torch.empty(sbp.attn_workspace_bytes(H, T, hd, chunk), dtype=torch.uint8, device="cuda")
+    dQ, dK, dV = torch.empty_like(ref["dQ"]), torch.empty_like(ref["dK"]), torch.empty_like(ref["dV"])
+    st = torch.zeros((), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(s):   # warm the library's per-device state outside the capture
+        sbp.attn_causal_backward(*args, dQ=dQ, dK=dK, dV=dV, workspace=ws, status=st, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sbp.attn_causal_backward(*args, dQ=dQ, dK=dK, dV=dV, workspace=ws, status=st, stream=s)
+    for x in (dQ, dK, dV):
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    sbp.check_status(st)
+    for k, x in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        assert torch.equal(x, ref[k]), k
+    # two host threads, two streams, two workspaces
+    outs = [None, None]
+
+    def run(i):
+        si = torch.cuda.Stream()
+        with torch.cuda.stream(si):
+            outs[i] = sbp.attn_causal_backward(*args, stream=si)
+        si.synchronize()
+    th = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    torch.cuda.synchronize()
+    for o in outs:
+        sbp.check_status(o["status"])
+        for k in ("dQ", "dK", "dV"):
+            assert torch.equal(o[k], ref[k]), k
