@@ -291,22 +291,32 @@ def run_ours(args):
     ms_per_step = ms / args.steps
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside ----
-    # (SFT call; for the other objectives the same copies wrap their step)
+    # SFT: the host-buffer entry point, which streams H in and dH out chunk by chunk
+    # beside the GEMMs; for the other objectives the same copies wrap their step
     Hh = torch.from_numpy(H).to(torch.bfloat16).pin_memory()
     yh = torch.from_numpy(y).pin_memory()
     dHh = torch.empty(Hh.shape, dtype=torch.bfloat16).pin_memory()
     lossh = torch.empty((), dtype=torch.float32).pin_memory()
-    Hd = torch.empty_like(Ht)
-    yd = torch.empty_like(yt)
+    nvh = torch.empty((), dtype=torch.int64).pin_memory()
+    if objective == "sft":
+        nh = sbp.host_workspace_bytes(T, d, V, chunk, sbp.BF16)
+        if lean:
+            nh -= sbp.workspace_bytes(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT) - \
+                sbp.workspace_bytes_lean(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT)
+        hws = torch.empty(nh, dtype=torch.uint8, device=dev)
+    else:
+        Hd = torch.empty_like(Ht)
+        yd = torch.empty_like(yt)
 
     def e2e_step():
+        if objective == "sft":
+            sbp.sft_host(Hh, Wt, yh, chunk, dH=dHh, dW=dW, loss=lossh, n_valid=nvh, workspace=hws, status=st,
+                         stream=stream)
+            return
         Hd.copy_(Hh, non_blocking=True)
         yd.copy_(yh, non_blocking=True)
-        if objective == "sft":
-            o = sbp.sft(Hd, Wt, yd, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False, stream=stream)
-        else:
-            Ht.copy_(Hd)
-            o = step()
+        Ht.copy_(Hd)
+        o = step()
         dHh.copy_(o["dH"], non_blocking=True)
         lossh.copy_(o["loss"], non_blocking=True)
 
@@ -325,7 +335,7 @@ def run_ours(args):
     sbp.check_status(st, "e2e region")
     e2e_tokens, e2e_ms = aggregate(torch, dist, float(T * args.steps), e2.elapsed_time(e3), dev)
     h2d = Hh.numel() * Hh.element_size() + yh.numel() * yh.element_size()
-    d2h = dHh.numel() * dHh.element_size() + lossh.element_size()
+    d2h = dHh.numel() * dHh.element_size() + lossh.element_size() + (nvh.element_size() if objective == "sft" else 0)
 
     if rank != 0:
         if dist is not None:
@@ -395,7 +405,9 @@ def run_ours(args):
         "peak_mem_gb": peak_mem / 1e9,
         "unchunked_fp32_logits_gb": T * V * 4 / 1e9,
         "e2e": {"value": e2e_tokens / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "call": ("sbp_lmhead_sft_host (H in and dH out per chunk, beside the GEMMs)" if objective == "sft"
+                         else "H2D copy, device call, D2H copy")},
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clk,
         "loss": loss,

@@ -264,6 +264,37 @@ int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels,
                            void* dH, float* dW, int accumulate_dW,
                            int32_t* dev_status, void* stream);
 
+/* SFT cross-entropy exactly as sbp_lmhead_sft (same kernels, same results bit for bit),
+ * with H, the labels and dH in HOST memory: the call streams them one chunk at a time,
+ * so that the device holds no [T, d] array.  This rests on the same chunk independence
+ * as the method itself (chunk c needs only its own rows of H, and produces only its own
+ * rows of dH); moving those rows in and out is a library convenience the pages do not
+ * describe.  Pipeline: the labels are copied in first (N is needed before the first
+ * gradient); chunk c's H rows are copied into one of three device slots of the workspace
+ * ahead of its forward GEMM, and its dH rows leave one of two slots for the host as soon
+ * as its backward GEMMs are done, while later chunks compute.  The copies run on the
+ * library's internal stream for this device, forked from `stream` and joined back into
+ * it within the call; the loss and N are copied to the host last, on `stream`.
+ *   H_host       [T, d] dtype, host memory, read       (page-locked for overlap)
+ *   labels_host  [T] int32, host memory, read
+ *   dH_host      [T, d] dtype, host memory, overwritten
+ *   loss_host    fp32, host memory (required);  n_valid_host  int64, host memory, nullable
+ *   W, dW, dev_status, workspace: device memory, as sbp_lmhead_sft.
+ * The host arrays must stay valid and untouched until `stream` has passed the call; read
+ * the outputs after synchronising it.  Page-locked (pinned) host memory lets the copies
+ * overlap the GEMMs; pageable memory gives the same results, with each copy out blocking
+ * the host until the device reaches it.  Workspace: at least
+ * sbp_lmhead_sft_host_workspace_bytes(...) for the default schedule, which is
+ * sbp_lmhead_workspace_bytes(..., SBP_MODE_SFT) plus 5 x chunk x d elements of row
+ * slots plus the labels; a smaller one large enough for one chunk buffer selects the
+ * one-buffer schedule, as for sbp_lmhead_sft.  Errors as sbp_lmhead_sft. */
+size_t sbp_lmhead_sft_host_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype);
+int sbp_lmhead_sft_host(const void* H_host, const void* W, const int32_t* labels_host,
+                        int64_t T, int64_t d, int64_t V, int64_t chunk, int32_t ignore_index,
+                        int dtype, float* loss_host, int64_t* n_valid_host,
+                        void* dH_host, float* dW, int accumulate_dW,
+                        void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* sbp_status_string(int status);
 

@@ -89,7 +89,8 @@ int choose_splits(int64_t rows, int64_t d, int64_t V, int sms) {
   return s;
 }
 
-bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L, int nbuf) {
+bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L, int nbuf,
+                 bool host) {
   if (T < 0 || d < 1 || V < 1 || chunk < 1 || chunk > 65535) return false;
   if (dtype != SBP_BF16 && dtype != SBP_FP32) return false;
   if (mode < SBP_MODE_SFT || mode > SBP_MODE_DPO2) return false;
@@ -120,6 +121,14 @@ bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int 
   l.off_seqw = o;    o = align256(o + (size_t)l.max_seq * sizeof(float));
   l.off_scal = o;    o = align256(o + 64);  // [0] int64 N
   l.off_cnt = o;     o = align256(o + (size_t)(l.n_chunks + 1) * sizeof(uint32_t));
+  if (host) {
+    const size_t slot = (size_t)l.chunk * d * l.esize;
+    l.host = true;
+    l.off_hs = o;    o = align256(o + 3 * slot);
+    l.off_dhs = o;   o = align256(o + 2 * slot);
+    l.off_y = o;     o = align256(o + (size_t)(T + 1) * sizeof(int32_t));
+    l.off_hscal = o; o = align256(o + 64);  // [0] fp32 loss, [8] int64 N
+  }
   l.total = o;
   *L = l;
   return true;
@@ -445,6 +454,51 @@ inline unsigned grid_for(int64_t work, int threads, int64_t cap = 4096) {
   return (unsigned)g;
 }
 
+// A second stream per device, for the work of one call that may run beside the caller's
+// stream: forked from it after an event and joined back into it before the call returns,
+// so the caller sees one ordered call on its own stream.  The lock is held while a call
+// enqueues its fork .. join, so concurrent calls never mix their events.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t ev[8] = {};   // handoffs inside a call (the LM head's host-buffer pipeline)
+  std::mutex mu;
+};
+static SideStream g_side[64];
+static std::mutex g_side_init;
+
+SideStream* side_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_side_init);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    for (cudaEvent_t& e : ss.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+      }
+    ss.s = st;
+    ss.fork = a;
+    ss.join = b;
+  }
+  return &ss;
+}
+
+// Host side of a streaming call: H [T, d] and the labels are read from host memory and
+// dH [T, d], the loss and N written to it; only a few chunks of rows are ever on the device.
+struct HostIO {
+  const void* H; const int32_t* labels; void* dH; float* loss; int64_t* n_valid;
+};
+
 struct Call {
   int mode;
   const void* H; const void* W; const int32_t* labels;
@@ -460,6 +514,7 @@ struct Call {
   float beta; double* margins;
   void* ws; size_t ws_bytes; int32_t* dev_status; cudaStream_t stream;
   int nbuf = 0;   // chunk buffer sets (0: default of make_layout)
+  const HostIO* host = nullptr;   // non-null: H, labels, dH, loss and N live in host memory
 };
 
 #define SBP_CUDA(x)                        \
@@ -471,19 +526,26 @@ struct Call {
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int validate(const Call& c, Layout* L) {
-  if (!make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, L, c.nbuf)) return SBP_ERR_INVALID_ARG;
+  const bool host = c.host != nullptr;
+  if (!make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, L, c.nbuf, host)) return SBP_ERR_INVALID_ARG;
   // a workspace too small for the default two chunk buffers but large enough for one
   // selects the one-buffer schedule (the logit gradient as its own pass per chunk)
   if (c.nbuf == 0 && L->nbuf == 2 && c.ws_bytes < L->total) {
     Layout lean;
-    if (make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, &lean, 1) && c.ws_bytes >= lean.total) *L = lean;
+    if (make_layout(c.T, c.d, c.V, c.chunk, c.dtype, c.mode, &lean, 1, host) && c.ws_bytes >= lean.total)
+      *L = lean;
   }
-  if (c.T > 0 && (!c.H || !c.labels)) return SBP_ERR_INVALID_ARG;
+  if (host) {
+    if (c.mode != SBP_MODE_SFT || !c.host->loss) return SBP_ERR_INVALID_ARG;
+    if (c.T > 0 && (!c.host->H || !c.host->labels || !c.host->dH)) return SBP_ERR_INVALID_ARG;
+  } else if (c.T > 0 && (!c.H || !c.labels)) {
+    return SBP_ERR_INVALID_ARG;
+  }
   if (!c.W || !c.dev_status) return SBP_ERR_INVALID_ARG;
   if (c.T > (int64_t)INT32_MAX) return SBP_ERR_UNSUPPORTED;
   const bool grad = c.mode != SBP_MODE_DPO1;
   if (grad && !c.dW) return SBP_ERR_INVALID_ARG;
-  if (grad && c.T > 0 && !c.dH) return SBP_ERR_INVALID_ARG;
+  if (grad && c.T > 0 && !c.dH && !host) return SBP_ERR_INVALID_ARG;
   if (c.mode == SBP_MODE_GRPO && c.T > 0 && (!c.adv || !c.logp_old)) return SBP_ERR_INVALID_ARG;
   if (c.mode == SBP_MODE_GRPO && !(c.clip_lo <= c.clip_hi)) return SBP_ERR_INVALID_ARG;
   if (c.mode == SBP_MODE_GRPO && c.kl_coef != 0.f && c.T > 0 && !c.ref_logp) return SBP_ERR_INVALID_ARG;
@@ -505,12 +567,12 @@ int validate(const Call& c, Layout* L) {
   return SBP_OK;
 }
 
-int run(const Call& c) {
+int run(const Call& cin) {
   Layout L;
-  int st = validate(c, &L);
+  int st = validate(cin, &L);
   if (st != SBP_OK) return st;
-  cudaStream_t s = c.stream;
-  char* ws = static_cast<char*>(c.ws);
+  cudaStream_t s = cin.stream;
+  char* ws = static_cast<char*>(cin.ws);
   void* zg = ws + L.off_zg;
   float2* part = reinterpret_cast<float2*>(ws + L.off_part);
   float* zy = reinterpret_cast<float*>(ws + L.off_zy);
@@ -523,7 +585,34 @@ int run(const Call& c) {
   uint32_t* counters = reinterpret_cast<uint32_t*>(ws + L.off_cnt);
   int launches = 0;
 
+  // Streaming host buffers: the labels, the loss and N go through the workspace, and the
+  // rows of H and dH through slots there, one chunk at a time, on the side stream:
+  // chunk j's H rows enter slot j % 3 ahead of its forward GEMM (at most three chunks
+  // ahead: a slot is refilled once its chunk's backward GEMMs are done), and its dH rows
+  // leave slot j % 2 for the host while later chunks compute.
+  const HostIO* hio = cin.host;
+  Call c = cin;
+  SideStream* ss = nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  const size_t row_bytes = (size_t)c.d * L.esize;
+  if (hio) {
+    c.labels = reinterpret_cast<const int32_t*>(ws + L.off_y);
+    c.loss = reinterpret_cast<float*>(ws + L.off_hscal);
+    c.n_valid = reinterpret_cast<int64_t*>(ws + L.off_hscal + 8);
+    ss = side_stream();
+    if (!ss) return SBP_ERR_CUDA;
+    side_lock = std::unique_lock<std::mutex>(ss->mu);
+  }
+  cudaEvent_t* ev_hready = hio ? ss->ev : nullptr;      // [3] chunk's H rows in their slot
+  cudaEvent_t* ev_bdone = hio ? ss->ev + 3 : nullptr;   // [2] chunk's backward done
+  cudaEvent_t* ev_dhfree = hio ? ss->ev + 5 : nullptr;  // [2] dH slot copied out
+  auto h_slot = [&](int64_t ci) { return ws + L.off_hs + (size_t)(ci % 3) * L.chunk * row_bytes; };
+  auto dh_slot = [&](int64_t ci) { return ws + L.off_dhs + (size_t)(ci % 2) * L.chunk * row_bytes; };
+
   SBP_CUDA(cudaMemsetAsync(c.dev_status, 0, sizeof(int32_t), s));
+  if (hio && c.T > 0)
+    SBP_CUDA(cudaMemcpyAsync(const_cast<int32_t*>(c.labels), hio->labels, (size_t)c.T * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, s));
   {
     prof::Scope ps(3, s);
     k_prep<<<1, 1024, 0, s>>>(c.labels, c.T, c.V, c.ign, nvalid, counters, L.n_chunks + 1, c.dev_status);
@@ -559,15 +648,33 @@ int run(const Call& c) {
     const int64_t r0 = r0_of(ci);
     return (int)((r0 + L.chunk <= c.T) ? L.chunk : c.T - r0);
   };
+  // where the GEMMs find chunk ci's H rows: the caller's H at row r0, or the chunk's slot
+  auto h_rows = [&](int64_t ci, const void** base, int64_t* T_map, int64_t* r0) {
+    if (hio) {
+      *base = h_slot(ci); *T_map = rows_of(ci); *r0 = 0;
+    } else {
+      *base = c.H; *T_map = c.T; *r0 = r0_of(ci);
+    }
+  };
+  // side stream: chunk j's H rows from the host into their slot
+  auto h_in = [&](int64_t j) -> int {
+    SBP_CUDA(cudaMemcpyAsync(h_slot(j), static_cast<const char*>(hio->H) + (size_t)r0_of(j) * row_bytes,
+                             (size_t)rows_of(j) * row_bytes, cudaMemcpyHostToDevice, ss->s));
+    SBP_CUDA(cudaEventRecord(ev_hready[j % 3], ss->s));
+    return SBP_OK;
+  };
 
   // forward GEMM + row statistics of chunk ci into buffer set b; on the tensor-core path it
   // also forms chunk `prev`'s gradient (buffer set pb) between its tiles when prev >= 0
   auto forward = [&](int64_t ci, int b, int64_t prev, int pb) -> int {
     const int64_t r0 = r0_of(ci);
     const int rows = rows_of(ci);
+    const void* hb; int64_t hT, hr0;
+    h_rows(ci, &hb, &hT, &hr0);
+    if (hio) SBP_CUDA(cudaStreamWaitEvent(s, ev_hready[ci % 3], 0));
     if (bf16) {
       TcFwdArgs a{};
-      a.H = c.H; a.W = c.W; a.T = c.T; a.d = c.d; a.V = c.V; a.r0 = r0; a.rows = rows;
+      a.H = hb; a.W = c.W; a.T = hT; a.d = c.d; a.V = c.V; a.r0 = hr0; a.rows = rows;
       a.labels = c.labels + r0; a.ignore_index = c.ign;
       a.E = grad ? zgb[b] : nullptr; a.lde = L.ldv; a.part = partb[b]; a.zy = zy; a.status = c.dev_status;
       if (prev >= 0) {
@@ -579,7 +686,7 @@ int run(const Call& c) {
       ++launches;
     } else {
       prof::Scope ps(0, s);
-      SBP_CUDA(simt_forward(static_cast<const float*>(c.H), static_cast<const float*>(c.W), c.d, c.V, r0, rows,
+      SBP_CUDA(simt_forward(static_cast<const float*>(hb), static_cast<const float*>(c.W), c.d, c.V, hr0, rows,
                             c.labels + r0, c.ign, static_cast<float*>(zgb[b]), L.ldv, partb[b], zy, grad, s));
       launches += 2;
     }
@@ -626,11 +733,15 @@ int run(const Call& c) {
     const int64_t r0 = r0_of(ci);
     const int rows = rows_of(ci);
     const int dw_acc = (ci > 0 || c.accumulate_dW) ? 1 : 0;
+    const void* hb; int64_t hT, hr0;
+    h_rows(ci, &hb, &hT, &hr0);
+    // the dH slot's previous chunk must have left for the host
+    if (hio && ci >= 2) SBP_CUDA(cudaStreamWaitEvent(s, ev_dhfree[ci % 2], 0));
     int splits = 1;
     if (bf16) {
       TcBwdArgs bw{};
-      bw.G = zgb[b]; bw.ldg = L.ldv; bw.H = c.H; bw.W = c.W; bw.T = c.T; bw.d = c.d; bw.V = c.V;
-      bw.r0 = r0; bw.rows = rows;
+      bw.G = zgb[b]; bw.ldg = L.ldv; bw.H = hb; bw.W = c.W; bw.T = hT; bw.d = c.d; bw.V = c.V;
+      bw.r0 = hr0; bw.rows = rows;
       splits = std::min(choose_splits(rows, c.d, c.V, num_sms()), L.splits);
       bw.splits = splits; bw.dh_part = dhp; bw.dW = c.dW; bw.dw_accumulate = dw_acc;
       bw.counter = counters + ci; bw.status = c.dev_status;
@@ -639,20 +750,34 @@ int run(const Call& c) {
       ++launches;
     } else {
       prof::Scope ps(1, s);
-      SBP_CUDA(simt_backward(static_cast<const float*>(zgb[b]), L.ldv, static_cast<const float*>(c.H),
-                             static_cast<const float*>(c.W), c.d, c.V, r0, rows, dhp, c.dW, dw_acc, s));
+      SBP_CUDA(simt_backward(static_cast<const float*>(zgb[b]), L.ldv, static_cast<const float*>(hb),
+                             static_cast<const float*>(c.W), c.d, c.V, hr0, rows, dhp, c.dW, dw_acc, s));
       launches += 2;
     }
     const int64_t n = (int64_t)rows * c.d;
-    prof::Scope ps(3, s);
-    if (bf16)
-      k_dh_reduce<__nv_bfloat16><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
-          dhp, splits, n, n, static_cast<__nv_bfloat16*>(c.dH) + r0 * c.d);
-    else
-      k_dh_reduce<float><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
-          dhp, splits, n, n, static_cast<float*>(c.dH) + r0 * c.d);
-    ++launches;
-    SBP_CUDA(cudaGetLastError());
+    void* dst = hio ? static_cast<void*>(dh_slot(ci)) : static_cast<char*>(c.dH) + (size_t)r0 * row_bytes;
+    {
+      prof::Scope ps(3, s);
+      if (bf16)
+        k_dh_reduce<__nv_bfloat16><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(
+            dhp, splits, n, n, static_cast<__nv_bfloat16*>(dst));
+      else
+        k_dh_reduce<float><<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(dhp, splits, n, n, static_cast<float*>(dst));
+      ++launches;
+      SBP_CUDA(cudaGetLastError());
+    }
+    if (hio) {
+      // side stream: dH rows out to the host, then the freed H slot takes chunk ci + 3
+      SBP_CUDA(cudaEventRecord(ev_bdone[ci % 2], s));
+      SBP_CUDA(cudaStreamWaitEvent(ss->s, ev_bdone[ci % 2], 0));
+      SBP_CUDA(cudaMemcpyAsync(static_cast<char*>(hio->dH) + (size_t)r0 * row_bytes, dst, (size_t)n * L.esize,
+                               cudaMemcpyDeviceToHost, ss->s));
+      SBP_CUDA(cudaEventRecord(ev_dhfree[ci % 2], ss->s));
+      if (ci + 3 < L.n_chunks) {
+        const int hs = h_in(ci + 3);
+        if (hs != SBP_OK) return hs;
+      }
+    }
     return SBP_OK;
   };
 
@@ -662,51 +787,74 @@ int run(const Call& c) {
     if (st_ != SBP_OK) return st_;      \
   } while (0)
 
-  if (!grad) {
-    for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
-      SBP_TRY(forward(ci, 0, -1, 0));
-      SBP_TRY(combine(ci, 0));
+  auto schedule = [&]() -> int {
+    if (hio) {
+      SBP_CUDA(cudaEventRecord(ss->fork, s));
+      SBP_CUDA(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+      for (int64_t j = 0; j < std::min<int64_t>(3, L.n_chunks); ++j) SBP_TRY(h_in(j));
     }
-  } else if (L.nbuf == 2 && bf16) {
-    // chunk ci's gradient forms inside chunk ci+1's forward (two buffer sets):
-    //   F0 C0 | F1(+G0) C1 B0 | F2(+G1) C2 B1 | ... | G_last B_last
-    SBP_TRY(forward(0, 0, -1, 0));
-    SBP_TRY(combine(0, 0));
-    for (int64_t ci = 1; ci < L.n_chunks; ++ci) {
-      const int b = (int)(ci & 1), pb = b ^ 1;
-      SBP_TRY(forward(ci, b, ci - 1, pb));
-      SBP_TRY(combine(ci, b));
-      SBP_TRY(backward(ci - 1, pb));
+    if (!grad) {
+      for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+        SBP_TRY(forward(ci, 0, -1, 0));
+        SBP_TRY(combine(ci, 0));
+      }
+    } else if (L.nbuf == 2 && bf16) {
+      // chunk ci's gradient forms inside chunk ci+1's forward (two buffer sets):
+      //   F0 C0 | F1(+G0) C1 B0 | F2(+G1) C2 B1 | ... | G_last B_last
+      SBP_TRY(forward(0, 0, -1, 0));
+      SBP_TRY(combine(0, 0));
+      for (int64_t ci = 1; ci < L.n_chunks; ++ci) {
+        const int b = (int)(ci & 1), pb = b ^ 1;
+        SBP_TRY(forward(ci, b, ci - 1, pb));
+        SBP_TRY(combine(ci, b));
+        SBP_TRY(backward(ci - 1, pb));
+      }
+      const int64_t last = L.n_chunks - 1;
+      if (last >= 0) {
+        SBP_TRY(gradient(last, (int)(last & 1)));
+        SBP_TRY(backward(last, (int)(last & 1)));
+      }
+    } else {
+      for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
+        SBP_TRY(forward(ci, 0, -1, 0));
+        SBP_TRY(combine(ci, 0));
+        SBP_TRY(gradient(ci, 0));
+        SBP_TRY(backward(ci, 0));
+      }
     }
-    const int64_t last = L.n_chunks - 1;
-    if (last >= 0) {
-      SBP_TRY(gradient(last, (int)(last & 1)));
-      SBP_TRY(backward(last, (int)(last & 1)));
+
+    if (c.mode == SBP_MODE_SFT || c.mode == SBP_MODE_GRPO) {
+      k_loss_final<<<1, 1024, 0, s>>>(tokloss, c.T, nvalid, c.loss, c.n_valid);
+      ++launches;
+    } else if (c.mode == SBP_MODE_DPO1) {
+      if (c.n_seq > 0) {
+        k_seq_sums<<<c.n_seq, 256, 0, s>>>(logp, c.cu, c.seq_logp);
+        ++launches;
+      }
+      if (c.n_valid) {
+        k_loss_final<<<1, 1024, 0, s>>>(tokloss, 0, nvalid, nullptr, c.n_valid);
+        ++launches;
+      }
     }
-  } else {
-    for (int64_t ci = 0; ci < L.n_chunks; ++ci) {
-      SBP_TRY(forward(ci, 0, -1, 0));
-      SBP_TRY(combine(ci, 0));
-      SBP_TRY(gradient(ci, 0));
-      SBP_TRY(backward(ci, 0));
-    }
-  }
+    SBP_CUDA(cudaGetLastError());
+    return SBP_OK;
+  };
 #undef SBP_TRY
 
-  if (c.mode == SBP_MODE_SFT || c.mode == SBP_MODE_GRPO) {
-    k_loss_final<<<1, 1024, 0, s>>>(tokloss, c.T, nvalid, c.loss, c.n_valid);
-    ++launches;
-  } else if (c.mode == SBP_MODE_DPO1) {
-    if (c.n_seq > 0) {
-      k_seq_sums<<<c.n_seq, 256, 0, s>>>(logp, c.cu, c.seq_logp);
-      ++launches;
-    }
-    if (c.n_valid) {
-      k_loss_final<<<1, 1024, 0, s>>>(tokloss, 0, nvalid, nullptr, c.n_valid);
-      ++launches;
+  st = schedule();
+  if (hio) {
+    // join the side stream back into the caller's stream whatever happened above, so
+    // that nothing of this call runs past it
+    const cudaError_t e1 = cudaEventRecord(ss->join, ss->s);
+    const cudaError_t e2 = cudaStreamWaitEvent(s, ss->join, 0);
+    if (st == SBP_OK && (e1 != cudaSuccess || e2 != cudaSuccess)) st = SBP_ERR_CUDA;
+    if (st == SBP_OK) {
+      SBP_CUDA(cudaMemcpyAsync(hio->loss, c.loss, sizeof(float), cudaMemcpyDeviceToHost, s));
+      if (hio->n_valid)
+        SBP_CUDA(cudaMemcpyAsync(hio->n_valid, c.n_valid, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
     }
   }
-  SBP_CUDA(cudaGetLastError());
+  if (st != SBP_OK) return st;
   if (c.logp_out && c.T > 0)
     SBP_CUDA(cudaMemcpyAsync(c.logp_out, logp, (size_t)c.T * sizeof(float), cudaMemcpyDeviceToDevice, s));
   g_launches = launches;
@@ -737,38 +885,6 @@ bool mlp_layout(int64_t T, int64_t d, int64_t f, int64_t chunk, MlpLayout* L) {
   return true;
 }
 
-// A second stream per device, for the work of one call that may run beside the caller's
-// stream: forked from it after an event and joined back into it before the call returns,
-// so the caller sees one ordered call on its own stream.  The lock is held while a call
-// enqueues its fork .. join, so concurrent calls never mix their events.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  std::mutex mu;
-};
-static SideStream g_side[64];
-static std::mutex g_side_init;
-
-SideStream* side_stream() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(g_side_init);
-  SideStream& ss = g_side[dev];
-  if (!ss.s) {
-    cudaStream_t st = nullptr;
-    cudaEvent_t a = nullptr, b = nullptr;
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    ss.s = st;
-    ss.fork = a;
-    ss.join = b;
-  }
-  return &ss;
-}
 
 int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int64_t T, int64_t d, int64_t f,
             int64_t chunk, void* dX, float* dWgu, float* dWd, int accumulate, void* ws, size_t ws_bytes,
@@ -1223,6 +1339,24 @@ int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels, 
   c.ws_bytes = (size_t)SBP_NOALLOC_SCRATCH_BYTES; c.dev_status = dev_status;
   c.stream = static_cast<cudaStream_t>(stream);
   c.nbuf = 1;   // one buffer set: the gradient of each chunk runs as its own pass
+  return run(c);
+}
+
+size_t sbp_lmhead_sft_host_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype) {
+  Layout L;
+  if (!make_layout(T, d, V, chunk, dtype, SBP_MODE_SFT, &L, 0, true)) return 0;
+  return L.total;
+}
+
+int sbp_lmhead_sft_host(const void* H_host, const void* W, const int32_t* labels_host, int64_t T, int64_t d,
+                        int64_t V, int64_t chunk, int32_t ignore_index, int dtype, float* loss_host,
+                        int64_t* n_valid_host, void* dH_host, float* dW, int accumulate_dW, void* workspace,
+                        size_t ws_bytes, int32_t* dev_status, void* stream) {
+  const HostIO io{H_host, labels_host, dH_host, loss_host, n_valid_host};
+  Call c{};
+  c.mode = SBP_MODE_SFT; c.W = W; c.T = T; c.d = d; c.V = V; c.chunk = chunk; c.ign = ignore_index;
+  c.dtype = dtype; c.dW = dW; c.accumulate_dW = accumulate_dW; c.ws = workspace; c.ws_bytes = ws_bytes;
+  c.dev_status = dev_status; c.stream = static_cast<cudaStream_t>(stream); c.host = &io;
   return run(c);
 }
 

@@ -27,12 +27,17 @@ struct Layout {
   size_t off_zg2 = 0, off_part2 = 0, off_rowv2 = 0;   // second buffer set (nbuf = 2)
   size_t off_tokloss = 0, off_logp = 0, off_seqw = 0, off_scal = 0, off_cnt = 0;
   int64_t n_chunks = 0, max_seq = 0;
+  // streaming host buffers (sbp_lmhead_sft_host): device slots for three chunks of H rows
+  // and two of dH rows, the labels [T] int32, and the loss / N scalars
+  bool host = false;
+  size_t off_hs = 0, off_dhs = 0, off_y = 0, off_hscal = 0;
   size_t total = 0;
 };
 
 // Fills `L`; returns false for arguments no call can accept.
 bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int mode, Layout* L,
-                 int nbuf = 0);   // 0: the entry points' default (2 for bf16 gradients, else 1)
+                 int nbuf = 0,    // 0: the entry points' default (2 for bf16 gradients, else 1)
+                 bool host = false);
 
 // dH split-K factor of the tensor-core backward kernel for a chunk of `rows` rows.
 int choose_splits(int64_t rows, int64_t d, int64_t V, int num_sms);

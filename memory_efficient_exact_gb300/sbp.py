@@ -57,6 +57,10 @@ def _load() -> ctypes.CDLL:
                                          SZ, P, P]
     lib.sbp_lmhead_sft_noalloc.restype = C
     lib.sbp_lmhead_sft_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, P, C, P, P]
+    lib.sbp_lmhead_sft_host_workspace_bytes.restype = SZ
+    lib.sbp_lmhead_sft_host_workspace_bytes.argtypes = [I64, I64, I64, I64, C]
+    lib.sbp_lmhead_sft_host.restype = C
+    lib.sbp_lmhead_sft_host.argtypes = [P, P, P, I64, I64, I64, I64, I32, C, P, P, P, P, C, P, SZ, P, P]
     lib.sbp_mlp_workspace_bytes.restype = SZ
     lib.sbp_mlp_workspace_bytes.argtypes = [I64, I64, I64, I64]
     lib.sbp_mlp_swiglu_backward.restype = C
@@ -222,6 +226,54 @@ def sft_noalloc(H, W, labels, chunk, ignore_index=IGNORE_INDEX, *, dH=None, dW=N
                                        _p(nv), _p(lp), _p(dH), _p(dW), int(bool(accumulate_dW)), _p(st),
                                        _stream(stream)), "sbp_lmhead_sft_noalloc")
     return dict(loss=loss, n_valid=nv, logp=lp, dH=dH, dW=dW, status=st)
+
+
+def host_workspace_bytes(T: int, d: int, V: int, chunk: int, dtype: int) -> int:
+    """Workspace of ``sft_host``: the SFT workspace plus the row slots and the labels."""
+    return int(_lib.sbp_lmhead_sft_host_workspace_bytes(T, d, V, chunk, dtype))
+
+
+def sft_host(H, W, labels, chunk, ignore_index=IGNORE_INDEX, *, dH=None, dW=None, accumulate_dW=False,
+             loss=None, n_valid=None, workspace=None, status=None, stream=None) -> dict:
+    """SFT forward + backward with H, labels, dH, loss and N in host memory
+    (``sbp_lmhead_sft_host``): the call streams the rows chunk by chunk.  H, labels and
+    the host outputs should be pinned for the copies to overlap the GEMMs; W, dW, the
+    workspace and the status are device tensors.  The host outputs are valid once the
+    stream has been synchronised."""
+    for t in (H, labels):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("H and labels must be contiguous host tensors")
+    _dev(W)
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    T, d = H.shape
+    V = W.shape[0]
+    if W.shape[1] != d or H.dtype != W.dtype or labels.shape != (T,):
+        raise ValueError("shape/dtype mismatch between H [T,d], W [V,d], labels [T]")
+    dt = _code(H)
+    pin = H.is_pinned()
+    if dH is None:
+        dH = torch.empty(H.shape, dtype=H.dtype, pin_memory=pin)
+    if dH.is_cuda or not dH.is_contiguous() or dH.shape != H.shape or dH.dtype != H.dtype:
+        raise ValueError("dH must be a contiguous host tensor shaped and typed like H")
+    if dW is None:
+        dW = torch.empty(W.shape, dtype=torch.float32, device=W.device)
+    _dev(dW)
+    if loss is None:
+        loss = torch.empty((), dtype=torch.float32, pin_memory=pin)
+    if n_valid is None:
+        n_valid = torch.empty((), dtype=torch.int64, pin_memory=pin)
+    if workspace is None:
+        n = host_workspace_bytes(T, d, V, chunk, dt)
+        if n == 0:
+            raise SbpError(ERR_INVALID_ARG, "sbp_lmhead_sft_host_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=W.device)
+    _dev(workspace)
+    st = torch.empty((), dtype=torch.int32, device=W.device) if status is None else status
+    _check(_lib.sbp_lmhead_sft_host(_p(H), _p(W), _p(labels), T, d, V, chunk, ignore_index, dt, _p(loss),
+                                    _p(n_valid), _p(dH), _p(dW), int(bool(accumulate_dW)), _p(workspace),
+                                    workspace.numel(), _p(st), _stream(stream)), "sbp_lmhead_sft_host")
+    return dict(loss=loss, n_valid=n_valid, dH=dH, dW=dW, status=st)
 
 
 def grpo(H, W, labels, advantages, logp_old, chunk, clip_lo=0.8, clip_hi=1.2, ignore_index=IGNORE_INDEX, *,

@@ -118,6 +118,46 @@ def test_argument_errors_are_caught_on_the_host(sbp):
     assert r == sbp.ERR_INVALID_ARG
 
 
+def test_host_stream_workspace(sbp):
+    # the host-buffer call needs the SFT workspace plus three H-row slots, two dH-row
+    # slots (chunk x d elements each) and the labels
+    T, d, V, C = 16384, 4096, 151936, 4096
+    base = sbp.workspace_bytes(T, d, V, C, sbp.BF16, sbp.MODE_SFT)
+    host = sbp.host_workspace_bytes(T, d, V, C, sbp.BF16)
+    assert 5 * C * d * 2 + 4 * T <= host - base <= 5 * C * d * 2 + 4 * T + 4 * 256
+    # fp32 slots hold fp32 rows; the chunk never exceeds T
+    b32 = sbp.workspace_bytes(100, 64, 1000, 4096, sbp.FP32, sbp.MODE_SFT)
+    h32 = sbp.host_workspace_bytes(100, 64, 1000, 4096, sbp.FP32)
+    assert 5 * 100 * 64 * 4 + 400 <= h32 - b32 <= 5 * 100 * 64 * 4 + 400 + 4 * 256
+    assert sbp.host_workspace_bytes(16, 0, 10, 4, sbp.BF16) == 0
+
+
+def test_host_stream_argument_errors(sbp):
+    # fails validation before any CUDA call: the fake addresses are never touched
+    lib = sbp._lib
+    P = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(H=0x1000, W=0x2000, y=0x3000, T=16, d=64, V=128, chunk=8, dtype=0, loss=0x4000, nv=None,
+                 dH=0x6000, dW=0x7000, ws=0x100000, wsb=1 << 30, st=0x8000)
+        a.update(kw)
+        return lib.sbp_lmhead_sft_host(P(a["H"]), P(a["W"]), P(a["y"]), a["T"], a["d"], a["V"], a["chunk"], -100,
+                                       a["dtype"], P(a["loss"]), P(a["nv"]), P(a["dH"]), P(a["dW"]), 0, P(a["ws"]),
+                                       a["wsb"], P(a["st"]), None)
+
+    assert call(loss=None) == sbp.ERR_INVALID_ARG
+    assert call(H=None) == sbp.ERR_INVALID_ARG
+    assert call(y=None) == sbp.ERR_INVALID_ARG
+    assert call(dH=None) == sbp.ERR_INVALID_ARG
+    assert call(W=None) == sbp.ERR_INVALID_ARG
+    assert call(dW=None) == sbp.ERR_INVALID_ARG
+    assert call(st=None) == sbp.ERR_INVALID_ARG
+    assert call(d=60) == sbp.ERR_UNSUPPORTED
+    assert call(W=0x2008) == sbp.ERR_ALIGNMENT
+    # the plain SFT workspace lacks the row slots
+    assert call(wsb=sbp.workspace_bytes(16, 64, 128, 8, sbp.BF16, sbp.MODE_SFT)) == sbp.ERR_WORKSPACE
+
+
 def test_product_path_never_imports_the_oracle():
     pkg = os.path.join(ROOT, "memory_efficient_exact_gb300")
     for dp, _, fs in os.walk(pkg):

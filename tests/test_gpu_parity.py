@@ -259,3 +259,69 @@ def test_label_out_of_range_sets_device_status(sbp):
     o = sbp.sft(Ht, Wt, yt, 16)
     torch.cuda.synchronize()
     assert int(o["status"].item()) == sbp.ERR_LABEL_RANGE
+
+
+HOST_CASES = [
+    # dtype, T, d, V, chunk, pinned
+    ("bf16", 700, 256, 3000, 128, True),     # 6 chunks: both slot rings wrap; ragged last chunk
+    ("bf16", 517, 192, 1304, 200, True),     # 3 chunks; chunk not a multiple of the 256-row tile
+    ("bf16", 300, 256, 2000, 1000, True),    # one chunk (chunk > T)
+    ("bf16", 1000, 512, 4096, 384, False),   # pageable host memory: same results
+    ("fp32", 77, 36, 531, 16, True),         # fp32 path, 5 chunks, ragged everything
+]
+
+
+@pytest.mark.parametrize("dtype,T,d,V,chunk,pinned", HOST_CASES)
+def test_sft_host_same_bits(sbp, dtype, T, d, V, chunk, pinned):
+    # H, labels and dH in host memory, streamed chunk by chunk through device slots: the
+    # same kernels on the same rows, so the same bits as the device-resident call
+    H, W, y = make_case(T, d, V, dtype, seed=21, w_std=0.08)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    ref = sbp.sft(Ht, Wt, yt, chunk, logp=False)
+    Hh, yh = Ht.cpu(), yt.cpu()
+    if pinned:
+        Hh, yh = Hh.pin_memory(), yh.pin_memory()
+    out = sbp.sft_host(Hh, Wt, yh, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    assert torch.equal(out["dH"], ref["dH"].cpu())
+    assert torch.equal(out["dW"], ref["dW"])
+    assert out["loss"].item() == ref["loss"].item()
+    assert int(out["n_valid"]) == int(ref["n_valid"].item())
+    # and against the oracle, as the device-resident call
+    o = O.sft(H, W, y, IGN)
+    assert rel(out["loss"].item(), o["loss"]) <= TOL[dtype]["loss"], (out["loss"].item(), o["loss"])
+
+
+def test_sft_host_lean_accumulate_and_empty(sbp):
+    T, d, V, chunk = 700, 256, 3000, 128
+    H, W, y = make_case(T, d, V, "bf16", seed=23, w_std=0.08)
+    Ht, Wt, yt = to_dev(torch, H, W, y, "bf16")
+    Hh, yh = Ht.cpu().pin_memory(), yt.cpu().pin_memory()
+    ref = sbp.sft(Ht, Wt, yt, chunk, logp=False)
+    # one-buffer schedule: the smallest accepted host workspace
+    full = sbp.host_workspace_bytes(T, d, V, chunk, sbp.BF16)
+    lean_dev = sbp.workspace_bytes_lean(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT)
+    dev_full = sbp.workspace_bytes(T, d, V, chunk, sbp.BF16, sbp.MODE_SFT)
+    lean = torch.empty(full - (dev_full - lean_dev), dtype=torch.uint8, device="cuda")
+    out = sbp.sft_host(Hh, Wt, yh, chunk, workspace=lean)
+    # accumulation into dW: twice the same batch
+    dW = torch.zeros(V, d, device="cuda")
+    sbp.sft_host(Hh, Wt, yh, chunk, dW=dW)
+    acc = sbp.sft_host(Hh, Wt, yh, chunk, dW=dW, accumulate_dW=True)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    assert torch.equal(out["dH"], ref["dH"].cpu()) and torch.equal(out["dW"], ref["dW"])
+    assert out["loss"].item() == ref["loss"].item()
+    ref2 = sbp.sft(Ht, Wt, yt, chunk, logp=False, dW=ref["dW"].clone(), accumulate_dW=True)
+    torch.cuda.synchronize()
+    assert torch.equal(acc["dW"], ref2["dW"])
+    # empty batch: dW overwritten with zeros, loss 0, N 0
+    He = torch.empty((0, d), dtype=torch.bfloat16).pin_memory()
+    ye = torch.empty((0,), dtype=torch.int32).pin_memory()
+    dW.fill_(7.0)
+    e = sbp.sft_host(He, Wt, ye, chunk, dW=dW)
+    torch.cuda.synchronize()
+    sbp.check_status(e["status"])
+    assert e["loss"].item() == 0.0 and int(e["n_valid"]) == 0
+    assert torch.count_nonzero(dW).item() == 0
