@@ -40,6 +40,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # backward kernel accumulates into dW as every launch but the first of a call does.
 PROFILE_WORKLOAD = dict(workload="sft_ce_lmhead_bf16_T8192_d4096_V32768_chunk4096", objective="sft", T=8192,
                         d=4096, V=32768, chunk=4096, dtype="bf16", seed=1002, mask="frac", frac=0.1)
+# The two chunk-sweep workloads (sizes and label masks of the named input recipes):
+# T = 8192 at d = 2560 with the first 1024 tokens masked as prompt, and the long-sequence
+# stress case T = 65536 at d = 5120 with 5% of the tokens ignored.
+SWEEP_WORKLOADS = {
+    "sft_T8192_d2560": dict(T=8192, d=2560, chunk=2048, seed=1001, mask="prefix", n=1024, frac=0.0),
+    "sft_T65536_d5120": dict(T=65536, d=5120, chunk=4096, seed=1004, mask="frac", frac=0.05),
+}
 CPU_SAMPLE_TOKENS = 384
 # DRAM bytes (read + write) of one accumulating k_bwd launch, from an ncu capture of the
 # profile workload (d = 4096, chunk 4096, V = 32768: 2.405 GB read + 0.566 GB written),
@@ -148,7 +155,7 @@ def make_inputs(rank: int, T: int | None = None):
     w = WORKLOAD
     T = w["T"] if T is None else T
     H, W = I.make_hw(T, w["d"], w["V"], w["seed"] + rank, w["dtype"])
-    y = I.make_labels(T, w["V"], w["seed"] + rank, w["mask"], w["frac"])
+    y = I.make_labels(T, w["V"], w["seed"] + rank, w["mask"], w["frac"], w.get("n", 0))
     return H, W, y
 
 
@@ -370,14 +377,15 @@ def run_ours(args):
         cpu = {"value": Ts / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"first {Ts} of the {T} tokens (full V={V}, d={d}), float64 numpy/BLAS, one run"}
 
-    metric = METRIC if objective == "sft" else f"lm_head fwd+bwd tokens/s ({objective}, d={d}, V={V})"
+    metric = METRIC if (objective, d, V) == ("sft", 4096, 151936) else \
+        f"lm_head fwd+bwd tokens/s ({objective}, d={d}, V={V})"
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w["workload"], "objective": objective, "T": T, "d": d, "V": V, "chunk": chunk,
                    "schedule": "one chunk buffer" if lean else "two chunk buffers",
-                   "tokens_per_gpu_per_step": T, "ignored_frac": w["frac"],
+                   "tokens_per_gpu_per_step": T, "ignored_frac": float(np.mean(y == -100)),
                    "l2": f"inputs larger than L2 (W {V * d * 2 / 1e9:.2f} GB; chunk logits "
                          f"{chunk * V * 2 / 1e9:.2f} GB per chunk)",
                    "parallelism": f"dp{world} replicas (no collective)"},
@@ -657,8 +665,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["main", "profile"], default="main",
-                    help="profile: a small case of the same kernels for ncu captures")
+    ap.add_argument("--workload", choices=["main", "profile"] + sorted(SWEEP_WORKLOADS), default="main",
+                    help="profile: a small case of the same kernels for ncu captures; "
+                         "sft_T8192_d2560 / sft_T65536_d5120: the chunk-sweep workloads (with --chunk)")
     ap.add_argument("--chunk", type=int, default=None, help="override the chunk size (sweeps)")
     ap.add_argument("--tokens", type=int, default=None, help="override T (sweeps)")
     ap.add_argument("--hd", type=int, default=None, help="override the attention head width (--sublayer attn)")
@@ -676,6 +685,11 @@ def main(argv=None):
         WORKLOAD.clear()
         WORKLOAD.update(PROFILE_WORKLOAD)
         args.no_cpu_baseline = True
+    if args.workload in SWEEP_WORKLOADS:
+        WORKLOAD.update(SWEEP_WORKLOADS[args.workload])
+        WORKLOAD["workload"] = "x"   # renamed below from the final sizes
+        if args.chunk is None:
+            args.chunk = WORKLOAD["chunk"]
     WORKLOAD["objective"] = args.objective
     if args.objective == "dpo" and args.tokens is None and args.workload == "main":
         WORKLOAD["T"] = 32768
