@@ -325,3 +325,54 @@ def test_sft_host_lean_accumulate_and_empty(sbp):
     sbp.check_status(e["status"])
     assert e["loss"].item() == 0.0 and int(e["n_valid"]) == 0
     assert torch.count_nonzero(dW).item() == 0
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16])
+def test_fp32_golden_fixtures(sbp, chunk):
+    # the stored oracle fixtures (tests/golden/, tiny odd sizes: d = 5, V = 11) through the
+    # fp32 path, in several chunks and with a chunk larger than T
+    import json
+    import os
+    gdir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    tol = TOL["fp32"]
+
+    def load(name):
+        fx = json.load(open(os.path.join(gdir, name)))
+        a = {k: (np.asarray(v) if isinstance(v, list) else v) for k, v in fx["inputs"].items()}
+        Ht, Wt, yt = to_dev(torch, a["H"].astype(np.float32), a["W"].astype(np.float32), a["labels"], "fp32")
+        return a, fx["outputs"], Ht, Wt, yt
+
+    def grads(out, want):
+        assert rel_fro(out["dH"].cpu().numpy(), want["dH"]) <= tol["grad"]
+        assert rel_fro(out["dW"].cpu().numpy(), want["dW"]) <= tol["grad"]
+
+    a, want, Ht, Wt, yt = load("lmhead_sft_T7_d5_V11.json")
+    o = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(o["status"])
+    assert int(o["n_valid"].item()) == want["n_valid"]
+    assert rel(o["loss"].item(), want["loss"]) <= tol["loss"]
+    assert np.max(np.abs(o["logp"].cpu().numpy() - np.asarray(want["logp"]))) <= tol["logp"]
+    grads(o, want)
+
+    a, want, Ht, Wt, yt = load("lmhead_grpo_T7_d5_V11.json")
+    At = torch.from_numpy(a["advantages"].astype(np.float32)).cuda()
+    lpo = torch.from_numpy(a["logp_old"].astype(np.float32)).cuda()
+    o = sbp.grpo(Ht, Wt, yt, At, lpo, chunk, a["clip_lo"], a["clip_hi"])
+    torch.cuda.synchronize()
+    sbp.check_status(o["status"])
+    assert int(o["n_valid"].item()) == want["n_valid"]
+    assert rel(o["loss"].item(), want["loss"]) <= tol["loss"]
+    grads(o, want)
+
+    a, want, Ht, Wt, yt = load("lmhead_dpo_T8_d5_V11.json")
+    cut = torch.from_numpy(a["cu_seqlens"].astype(np.int32)).cuda()
+    p1 = sbp.dpo_pass1(Ht, Wt, yt, cut, chunk)
+    p2 = sbp.dpo_pass2(Ht, Wt, yt, cut, p1["seq_logp"], torch.from_numpy(a["ref_seq_logp"]).cuda(), a["beta"],
+                       chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(p2["status"])
+    S = np.asarray(want["seq_logp"])
+    assert np.max(np.abs(p1["seq_logp"].cpu().numpy() - S) / np.abs(S)) <= tol["seq"]
+    assert rel(p2["loss"].item(), want["loss"]) <= tol["loss"]
+    grads(p2, want)
