@@ -56,3 +56,40 @@ def test_two_rank_aggregation_over_gloo():
         assert ms == 15.0                # max over ranks
         assert n_ign == 6                # floor(0.1 * 64) on every rank
     assert res[0][6] != res[1][6]        # each rank draws its own batch
+
+
+def _args_of(argv):
+    """The workload bench.main() would run for argv (the run is replaced by a recorder)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_args_probe", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    seen = {}
+
+    def rec(args):
+        seen.update(dict(b.WORKLOAD), chunk_arg=args.chunk, sublayer=args.sublayer)
+        return 0
+    b.run_ours = b.run_mlp_bench = b.run_attn_bench = rec
+    b.run_reference = rec
+    assert b.main(argv) == 0
+    return seen
+
+
+def test_bench_workload_selection():
+    # default: the SFT workload the metric is quoted on
+    w = _args_of([])
+    assert (w["T"], w["d"], w["V"], w["chunk"], w["objective"]) == (16384, 4096, 151936, 4096, "sft")
+    assert w["workload"] == "sft_ce_lmhead_bf16_T16384_d4096_V151936_chunk4096"
+    # the two chunk-sweep workloads keep their sizes and label masks
+    w = _args_of(["--workload", "sft_T8192_d2560", "--chunk", "512"])
+    assert (w["T"], w["d"], w["chunk"], w["mask"], w["n"]) == (8192, 2560, 512, "prefix", 1024)
+    assert w["workload"] == "sft_ce_lmhead_bf16_T8192_d2560_V151936_chunk512"
+    w = _args_of(["--workload", "sft_T65536_d5120"])
+    assert (w["T"], w["d"], w["chunk"], w["mask"], w["frac"]) == (65536, 5120, 4096, "frac", 0.05)
+    # DPO defaults to 8 sequences of 4096 tokens; GRPO keeps 8 x 2048
+    assert _args_of(["--objective", "dpo"])["T"] == 32768
+    assert _args_of(["--objective", "grpo"])["T"] == 16384
+    # the profile case for ncu captures
+    w = _args_of(["--workload", "profile"])
+    assert (w["T"], w["V"], w["chunk"]) == (8192, 32768, 4096)
+    assert _args_of(["--sublayer", "attn"])["sublayer"] == "attn"
