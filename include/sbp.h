@@ -283,7 +283,8 @@ int sbp_lmhead_sft_noalloc(const void* H, const void* W, const int32_t* labels,
  * The host arrays must stay valid and untouched until `stream` has passed the call; read
  * the outputs after synchronising it.  Page-locked (pinned) host memory lets the copies
  * overlap the GEMMs; pageable memory gives the same results, with each copy out blocking
- * the host until the device reaches it.  Workspace: at least
+ * the host until the device reaches it (and cannot be captured into a CUDA graph: under
+ * stream capture the host arrays must be page-locked).  Workspace: at least
  * sbp_lmhead_sft_host_workspace_bytes(...) for the default schedule, which is
  * sbp_lmhead_workspace_bytes(..., SBP_MODE_SFT) plus 5 x chunk x d elements of row
  * slots plus the labels; a smaller one large enough for one chunk buffer selects the
