@@ -64,6 +64,8 @@ extern "C" {
 #define SBP_ERR_CUDA 6          /* a CUDA runtime call failed (launch, memset, ...)       */
 #define SBP_ERR_UNSUPPORTED 7   /* shape the kernels do not handle (see dtype rules)       */
 #define SBP_ERR_SCRATCH_LIMIT 8 /* sizes need more scratch than sbp_lmhead_sft_noalloc has */
+#define SBP_ERR_WORKSPACE_OVERRUN 9 /* (device, checked build only) a kernel wrote into a guard
+                                       zone between workspace regions                     */
 
 /* operand dtypes */
 #define SBP_BF16 0

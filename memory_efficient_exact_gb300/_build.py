@@ -1,4 +1,12 @@
-"""Builds libsbp.so in-tree with nvcc for sm_103a (one object per .cu, compiled in parallel)."""
+"""Builds libsbp.so in-tree with nvcc for sm_103a (one object per .cu, compiled in parallel).
+
+Variants of the same sources (each its own objects and library, selected at import time
+by the SBP_LIBRARY_VARIANT environment variable):
+  ""         libsbp.so          the library
+  "checked"  libsbp_checked.so  guard zones after every workspace region, verified after
+                                each call (SBP_ERR_WORKSPACE_OVERRUN); -DSBP_CHECKED
+  "nvtx"     libsbp_nvtx.so     NVTX ranges per call and phase; -DSBP_NVTX
+"""
 from __future__ import annotations
 
 import os
@@ -15,6 +23,18 @@ SOURCES = ["sbp_api.cu", "sbp_simt.cu", "sbp_tc.cu", "sbp_mlp.cu", "sbp_attn.cu"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include"),
          "--expt-relaxed-constexpr"]
+VARIANTS = {"": [], "checked": ["-DSBP_CHECKED"], "nvtx": ["-DSBP_NVTX"]}
+
+
+def current_variant() -> str:
+    """The variant this process loads (SBP_LIBRARY_VARIANT, default "")."""
+    return os.environ.get("SBP_LIBRARY_VARIANT", "")
+
+
+def lib_path(variant: str = "") -> str:
+    if variant not in VARIANTS:
+        raise ValueError(f"unknown library variant {variant!r} (one of {sorted(VARIANTS)})")
+    return LIB if not variant else os.path.join(PKG, f"libsbp_{variant}.so")
 
 
 def nvcc() -> str:
@@ -24,8 +44,8 @@ def nvcc() -> str:
     return exe
 
 
-def _compile(src: str, extra) -> str:
-    out = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra, obj_dir: str) -> str:
+    out = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", out]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -33,29 +53,35 @@ def _compile(src: str, extra) -> str:
     return out
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "sbp.h"),
                                                                  os.path.abspath(__file__)]
     return any(os.path.getmtime(p) > t for p in deps if os.path.exists(p))
 
 
-def build_library(force: bool = False, extra=()) -> str:
-    """Compile every CUDA source of the library and link libsbp.so; returns its path."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(OBJ, exist_ok=True)
+def build_library(force: bool = False, extra=(), variant: str | None = None) -> str:
+    """Compile every CUDA source of the library and link libsbp.so, or the variant's
+    library (by default the one this process loads); returns its path."""
+    if variant is None:
+        variant = current_variant()
+    lib = lib_path(variant)
+    if not force and not _stale(lib):
+        return lib
+    obj_dir = os.path.join(OBJ, variant) if variant else OBJ
+    os.makedirs(obj_dir, exist_ok=True)
+    flags = VARIANTS[variant] + list(extra)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra)), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, flags, obj_dir), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

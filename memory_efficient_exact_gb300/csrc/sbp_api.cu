@@ -63,8 +63,6 @@ struct Scope {
 };
 }  // namespace prof
 
-static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -106,28 +104,29 @@ bool make_layout(int64_t T, int64_t d, int64_t V, int64_t chunk, int dtype, int 
   if (nbuf == 0) nbuf = (dtype == SBP_BF16 && mode != SBP_MODE_DPO1 && l.n_chunks > 1) ? 2 : 1;
   l.nbuf = nbuf;
   size_t o = 0;
-  l.off_zg = o;      o = align256(o + (size_t)l.chunk * l.ldv * l.esize);
-  l.off_part = o;    o = align256(o + (size_t)l.chunk * l.ntiles * sizeof(float2));
-  l.off_zy = o;      o = align256(o + (size_t)l.chunk * sizeof(float));
-  l.off_rowv = o;    o = align256(o + (size_t)l.chunk * sizeof(float));
+  Guards& g = l.guards;
+  l.off_zg = take_region(o, (size_t)l.chunk * l.ldv * l.esize, g);
+  l.off_part = take_region(o, (size_t)l.chunk * l.ntiles * sizeof(float2), g);
+  l.off_zy = take_region(o, (size_t)l.chunk * sizeof(float), g);
+  l.off_rowv = take_region(o, (size_t)l.chunk * sizeof(float), g);
   if (nbuf == 2) {
-    l.off_zg2 = o;   o = align256(o + (size_t)l.chunk * l.ldv * l.esize);
-    l.off_part2 = o; o = align256(o + (size_t)l.chunk * l.ntiles * sizeof(float2));
-    l.off_rowv2 = o; o = align256(o + (size_t)l.chunk * sizeof(float));
+    l.off_zg2 = take_region(o, (size_t)l.chunk * l.ldv * l.esize, g);
+    l.off_part2 = take_region(o, (size_t)l.chunk * l.ntiles * sizeof(float2), g);
+    l.off_rowv2 = take_region(o, (size_t)l.chunk * sizeof(float), g);
   }
-  l.off_dhp = o;     o = align256(o + (size_t)l.splits * l.chunk * d * sizeof(float));
-  l.off_tokloss = o; o = align256(o + (size_t)(T + 1) * sizeof(float));
-  l.off_logp = o;    o = align256(o + (size_t)(T + 1) * sizeof(float));
-  l.off_seqw = o;    o = align256(o + (size_t)l.max_seq * sizeof(float));
-  l.off_scal = o;    o = align256(o + 64);  // [0] int64 N
-  l.off_cnt = o;     o = align256(o + (size_t)(l.n_chunks + 1) * sizeof(uint32_t));
+  l.off_dhp = take_region(o, (size_t)l.splits * l.chunk * d * sizeof(float), g);
+  l.off_tokloss = take_region(o, (size_t)(T + 1) * sizeof(float), g);
+  l.off_logp = take_region(o, (size_t)(T + 1) * sizeof(float), g);
+  l.off_seqw = take_region(o, (size_t)l.max_seq * sizeof(float), g);
+  l.off_scal = take_region(o, 64, g);  // [0] int64 N
+  l.off_cnt = take_region(o, (size_t)(l.n_chunks + 1) * sizeof(uint32_t), g);
   if (host) {
     const size_t slot = (size_t)l.chunk * d * l.esize;
     l.host = true;
-    l.off_hs = o;    o = align256(o + 3 * slot);
-    l.off_dhs = o;   o = align256(o + 2 * slot);
-    l.off_y = o;     o = align256(o + (size_t)(T + 1) * sizeof(int32_t));
-    l.off_hscal = o; o = align256(o + 64);  // [0] fp32 loss, [8] int64 N
+    l.off_hs = take_region(o, 3 * slot, g);
+    l.off_dhs = take_region(o, 2 * slot, g);
+    l.off_y = take_region(o, (size_t)(T + 1) * sizeof(int32_t), g);
+    l.off_hscal = take_region(o, 64, g);  // [0] fp32 loss, [8] int64 N
   }
   l.total = o;
   *L = l;
@@ -442,6 +441,43 @@ __global__ void k_dpo_scales(const double* __restrict__ S, const double* __restr
   if (loss) *loss = P > 0 ? (float)(L / (double)P) : 0.f;
 }
 
+#ifdef SBP_CHECKED
+// Guard zone z holds the words 0x5BADF00D ^ (z << 16) ^ i; `skew` (the SBP_FAULT_GUARD
+// test knob) plants a wrong first word in the last zone, standing in for an overrun.
+__global__ void __launch_bounds__(64) k_guard(unsigned char* ws, Guards g, int check, uint32_t skew,
+                                              int32_t* status) {
+  const int z = blockIdx.x;
+  if (z >= g.n) return;
+  uint32_t* p = reinterpret_cast<uint32_t*>(ws + g.off[z]);
+  for (int i = threadIdx.x; i < (int)(kGuardBytes / 4); i += blockDim.x) {
+    const uint32_t want = 0x5BADF00Du ^ ((uint32_t)z << 16) ^ (uint32_t)i;
+    if (!check)
+      p[i] = want + ((z == g.n - 1 && i == 0) ? skew : 0u);
+    else if (p[i] != want)
+      set_status(status, SBP_ERR_WORKSPACE_OVERRUN);
+  }
+}
+#endif
+
+// Fills (check = 0) or verifies (check = 1) a workspace's guard zones on stream s; nothing
+// in the release build, whose layouts have no guard zones.
+int guard_zones(void* ws, const Guards& g, int check, int32_t* status, cudaStream_t s, int* launches) {
+#ifdef SBP_CHECKED
+  if (g.n == 0) return SBP_OK;
+  uint32_t skew = 0;
+  if (!check) {
+    const char* e = std::getenv("SBP_FAULT_GUARD");
+    skew = (e && e[0] == '1') ? 1u : 0u;
+  }
+  k_guard<<<g.n, 64, 0, s>>>(static_cast<unsigned char*>(ws), g, check, skew, status);
+  ++*launches;
+  return cudaGetLastError() == cudaSuccess ? SBP_OK : SBP_ERR_CUDA;
+#else
+  (void)ws; (void)g; (void)check; (void)status; (void)s; (void)launches;
+  return SBP_OK;
+#endif
+}
+
 __global__ void k_zero_f32(float* p, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     p[i] = 0.f;
@@ -609,7 +645,10 @@ int run(const Call& cin) {
   auto h_slot = [&](int64_t ci) { return ws + L.off_hs + (size_t)(ci % 3) * L.chunk * row_bytes; };
   auto dh_slot = [&](int64_t ci) { return ws + L.off_dhs + (size_t)(ci % 2) * L.chunk * row_bytes; };
 
+  NvtxRange nv_call("sbp_lmhead");
   SBP_CUDA(cudaMemsetAsync(c.dev_status, 0, sizeof(int32_t), s));
+  st = guard_zones(ws, L.guards, 0, c.dev_status, s, &launches);
+  if (st != SBP_OK) return st;
   if (hio && c.T > 0)
     SBP_CUDA(cudaMemcpyAsync(const_cast<int32_t*>(c.labels), hio->labels, (size_t)c.T * sizeof(int32_t),
                              cudaMemcpyHostToDevice, s));
@@ -667,6 +706,7 @@ int run(const Call& cin) {
   // forward GEMM + row statistics of chunk ci into buffer set b; on the tensor-core path it
   // also forms chunk `prev`'s gradient (buffer set pb) between its tiles when prev >= 0
   auto forward = [&](int64_t ci, int b, int64_t prev, int pb) -> int {
+    NvtxRange nv("forward");
     const int64_t r0 = r0_of(ci);
     const int rows = rows_of(ci);
     const void* hb; int64_t hT, hr0;
@@ -694,6 +734,7 @@ int run(const Call& cin) {
   };
   // lse, logp, weights, loss terms; the tile maxima become gradient scales
   auto combine = [&](int64_t ci, int b) -> int {
+    NvtxRange nv("combine");
     const int64_t r0 = r0_of(ci);
     const int rows = rows_of(ci);
     CombineArgs ca{};
@@ -716,6 +757,7 @@ int run(const Call& cin) {
   };
   // standalone logit gradient, in place
   auto gradient = [&](int64_t ci, int b) -> int {
+    NvtxRange nv("gradient");
     const int64_t vec = (c.V + 7) / 8;
     dim3 g((unsigned)((vec + 255) / 256), (unsigned)rows_of(ci));
     prof::Scope ps(2, s);
@@ -730,6 +772,7 @@ int run(const Call& cin) {
   };
   // dH_c = G_c W and dW (+)= G_c^T H_c, then dH_c's split partials -> dH rows
   auto backward = [&](int64_t ci, int b) -> int {
+    NvtxRange nv("backward");
     const int64_t r0 = r0_of(ci);
     const int rows = rows_of(ci);
     const int dw_acc = (ci > 0 || c.accumulate_dW) ? 1 : 0;
@@ -848,6 +891,7 @@ int run(const Call& cin) {
     const cudaError_t e1 = cudaEventRecord(ss->join, ss->s);
     const cudaError_t e2 = cudaStreamWaitEvent(s, ss->join, 0);
     if (st == SBP_OK && (e1 != cudaSuccess || e2 != cudaSuccess)) st = SBP_ERR_CUDA;
+    if (st == SBP_OK) st = guard_zones(ws, L.guards, 1, c.dev_status, s, &launches);
     if (st == SBP_OK) {
       SBP_CUDA(cudaMemcpyAsync(hio->loss, c.loss, sizeof(float), cudaMemcpyDeviceToHost, s));
       if (hio->n_valid)
@@ -855,6 +899,10 @@ int run(const Call& cin) {
     }
   }
   if (st != SBP_OK) return st;
+  if (!hio) {
+    st = guard_zones(ws, L.guards, 1, c.dev_status, s, &launches);
+    if (st != SBP_OK) return st;
+  }
   if (c.logp_out && c.T > 0)
     SBP_CUDA(cudaMemcpyAsync(c.logp_out, logp, (size_t)c.T * sizeof(float), cudaMemcpyDeviceToDevice, s));
   g_launches = launches;
@@ -867,6 +915,7 @@ struct MlpLayout {
   int64_t chunk = 0, n_chunks = 0;
   int splits = 1;
   size_t off_gu = 0, off_a = 0, off_dhp = 0, off_cnt = 0, total = 0;
+  Guards guards;   // checked build only
 };
 
 bool mlp_layout(int64_t T, int64_t d, int64_t f, int64_t chunk, MlpLayout* L) {
@@ -876,10 +925,10 @@ bool mlp_layout(int64_t T, int64_t d, int64_t f, int64_t chunk, MlpLayout* L) {
   l.n_chunks = T > 0 ? (T + l.chunk - 1) / l.chunk : 0;
   l.splits = choose_splits(l.chunk, d, 2 * f, num_sms());
   size_t o = 0;
-  l.off_gu = o;  o = align256(o + (size_t)l.chunk * 2 * f * 2);
-  l.off_a = o;   o = align256(o + (size_t)l.chunk * f * 2);
-  l.off_dhp = o; o = align256(o + (size_t)l.splits * l.chunk * d * sizeof(float));
-  l.off_cnt = o; o = align256(o + (size_t)(2 * l.n_chunks + 1) * sizeof(uint32_t));
+  l.off_gu = take_region(o, (size_t)l.chunk * 2 * f * 2, l.guards);
+  l.off_a = take_region(o, (size_t)l.chunk * f * 2, l.guards);
+  l.off_dhp = take_region(o, (size_t)l.splits * l.chunk * d * sizeof(float), l.guards);
+  l.off_cnt = take_region(o, (size_t)(2 * l.n_chunks + 1) * sizeof(uint32_t), l.guards);
   l.total = o;
   *L = l;
   return true;
@@ -903,7 +952,12 @@ int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int6
   float* dhp = reinterpret_cast<float*>(w + L.off_dhp);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(w + L.off_cnt);
   int launches = 0;
+  NvtxRange nv_call("sbp_mlp");
   SBP_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
+  {
+    const int gs = guard_zones(ws, L.guards, 0, dev_status, s, &launches);
+    if (gs != SBP_OK) return gs;
+  }
   SBP_CUDA(cudaMemsetAsync(cnt, 0, (size_t)(2 * L.n_chunks + 1) * sizeof(uint32_t), s));
   if (T == 0 && !accumulate) {
     k_zero_f32<<<grid_for(2 * f * d, 256), 256, 0, s>>>(dWgu, 2 * f * d);
@@ -981,6 +1035,7 @@ int run_mlp(const void* X, const void* Wgu, const void* Wd, const void* dY, int6
     if (cudaEventRecord(ss->join, se) != cudaSuccess || cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess)
       rc = SBP_ERR_CUDA;
   }
+  if (rc == SBP_OK) rc = guard_zones(ws, L.guards, 1, dev_status, s, &launches);
   if (rc != SBP_OK) return rc;
   g_launches = launches;
   return SBP_OK;
@@ -1019,6 +1074,7 @@ struct AttnLayout {
   int splits = 1;
   bool fused = false;   // hd = 128: P and dS stay on chip, the workspace holds D only
   size_t off_p = 0, off_ds = 0, off_d = 0, off_dqp = 0, off_cnt = 0, total = 0;
+  Guards guards;   // checked build only
 };
 
 int attn_splits(int64_t rows, int64_t hd, int64_t L, int H) {
@@ -1043,16 +1099,16 @@ bool attn_layout(int64_t H, int64_t T, int64_t hd, int64_t chunk, AttnLayout* L)
   l.fused = hd == 128;
   size_t o = 0;
   if (l.fused) {
-    l.off_d = o; o = align256(o + (size_t)H * std::max<int64_t>(T, 1) * sizeof(float));
+    l.off_d = take_region(o, (size_t)H * std::max<int64_t>(T, 1) * sizeof(float), l.guards);
     l.total = o;
     *L = l;
     return true;
   }
-  l.off_p = o;   o = align256(o + (size_t)H * l.Cmax * l.Lp * 2);
-  l.off_ds = o;  o = align256(o + (size_t)H * l.Cmax * l.Lp * 2);
-  l.off_d = o;   o = align256(o + (size_t)H * std::max<int64_t>(T, 1) * sizeof(float));
-  l.off_dqp = o; o = align256(o + (size_t)l.splits * H * l.Cmax * hd * sizeof(float));
-  l.off_cnt = o; o = align256(o + (size_t)(2 * l.n_chunks + 1) * sizeof(uint32_t));
+  l.off_p = take_region(o, (size_t)H * l.Cmax * l.Lp * 2, l.guards);
+  l.off_ds = take_region(o, (size_t)H * l.Cmax * l.Lp * 2, l.guards);
+  l.off_d = take_region(o, (size_t)H * std::max<int64_t>(T, 1) * sizeof(float), l.guards);
+  l.off_dqp = take_region(o, (size_t)l.splits * H * l.Cmax * hd * sizeof(float), l.guards);
+  l.off_cnt = take_region(o, (size_t)(2 * l.n_chunks + 1) * sizeof(uint32_t), l.guards);
   l.total = o;
   *L = l;
   return true;
@@ -1119,6 +1175,10 @@ int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, 
   return SBP_OK;
 }
 
+int run_attn_chunks(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
+                    int64_t H, int64_t T, int64_t hd, float scale, const AttnLayout& L, void* dQ, float* dK,
+                    float* dV, int accumulate, char* w, int32_t* dev_status, cudaStream_t s);
+
 int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
              int64_t H, int64_t Hkv, int64_t T, int64_t hd, float scale, int64_t chunk, void* dQ, float* dK,
              float* dV, int accumulate, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t s) {
@@ -1133,8 +1193,21 @@ int run_attn(const void* Q, const void* K, const void* Vv, const void* O, const 
     if (q && !al16(q)) return SBP_ERR_ALIGNMENT;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return SBP_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
-  if (L.fused)
-    return run_attn_fused(Q, K, Vv, O, dO, lse, H, Hkv, T, scale, L, dQ, dK, dV, accumulate, w, dev_status, s);
+  NvtxRange nv_call("sbp_attn");
+  int gl = 0;
+  int rc = guard_zones(w, L.guards, 0, dev_status, s, &gl);
+  if (rc != SBP_OK) return rc;
+  rc = L.fused ? run_attn_fused(Q, K, Vv, O, dO, lse, H, Hkv, T, scale, L, dQ, dK, dV, accumulate, w, dev_status, s)
+               : run_attn_chunks(Q, K, Vv, O, dO, lse, H, T, hd, scale, L, dQ, dK, dV, accumulate, w, dev_status, s);
+  if (rc == SBP_OK) rc = guard_zones(w, L.guards, 1, dev_status, s, &gl);
+  if (rc == SBP_OK) g_launches += gl;
+  return rc;
+}
+
+// other head widths: per chunk, P and dS through chunk buffers in the workspace
+int run_attn_chunks(const void* Q, const void* K, const void* Vv, const void* O, const void* dO, const float* lse,
+                    int64_t H, int64_t T, int64_t hd, float scale, const AttnLayout& L, void* dQ, float* dK,
+                    float* dV, int accumulate, char* w, int32_t* dev_status, cudaStream_t s) {
   void* pbuf = w + L.off_p;
   void* dsbuf = w + L.off_ds;
   float* D = reinterpret_cast<float*>(w + L.off_d);
@@ -1406,6 +1479,7 @@ const char* sbp_status_string(int status) {
     case SBP_ERR_CUDA: return "SBP_ERR_CUDA";
     case SBP_ERR_UNSUPPORTED: return "SBP_ERR_UNSUPPORTED";
     case SBP_ERR_SCRATCH_LIMIT: return "SBP_ERR_SCRATCH_LIMIT";
+    case SBP_ERR_WORKSPACE_OVERRUN: return "SBP_ERR_WORKSPACE_OVERRUN";
     default: return "SBP_ERR_UNKNOWN";
   }
 }
@@ -1424,7 +1498,7 @@ int sbp_profile_read(double* ms, int64_t* launches, int n) {
   for (auto& p : *prof::g_pairs) {
     float t = 0.f;
     if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&t, p.a, p.b) != cudaSuccess) err = 1;
-    if (p.cls < n) {
+    if (p.cls < n && p.cls < prof::kClasses) {
       if (ms) ms[p.cls] += (double)t;
       if (launches) launches[p.cls] += 1;
     }

@@ -14,6 +14,50 @@ namespace sbp {
 // one partial (max, sum of exp) and one gradient scale.
 constexpr int kStatW = 128;
 
+// Guard zones of the checked build (compiled with SBP_CHECKED): every workspace region is
+// followed by kGuardBytes holding a known pattern, written by the call before its first
+// kernel and verified after its last one; a mismatch (a kernel wrote past its region)
+// sets SBP_ERR_WORKSPACE_OVERRUN.  The release build has no guard zones.
+#ifdef SBP_CHECKED
+constexpr size_t kGuardBytes = 256;
+#else
+constexpr size_t kGuardBytes = 0;
+#endif
+constexpr int kMaxGuards = 24;
+struct Guards {
+  int n = 0;
+  size_t off[kMaxGuards] = {};
+};
+
+// The next workspace region of `bytes` at offset o (256-byte aligned); o moves past the
+// region and, in the checked build, past the region's guard zone.
+inline size_t take_region(size_t& o, size_t bytes, Guards& g) {
+  const size_t at = o;
+  o = (o + bytes + 255) & ~size_t(255);
+  if (kGuardBytes && g.n < kMaxGuards) {
+    g.off[g.n++] = o;
+    o += kGuardBytes;
+  }
+  return at;
+}
+
+// NVTX ranges around each call and its phases in the NVTX build (SBP_NVTX); nothing in
+// the others.  The ranges mark the host's enqueueing; a timeline tool pairs them with
+// the launches they contain.
+#ifdef SBP_NVTX
+#include <nvtx3/nvToolsExt.h>
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#else
+struct NvtxRange {
+  explicit NvtxRange(const char*) {}
+};
+#endif
+
 // Workspace carve-up.  Every region starts on a 256-byte boundary.
 struct Layout {
   int64_t T = 0, d = 0, V = 0, chunk = 0;  // chunk = rows of the largest chunk (<= T)
@@ -32,6 +76,7 @@ struct Layout {
   bool host = false;
   size_t off_hs = 0, off_dhs = 0, off_y = 0, off_hscal = 0;
   size_t total = 0;
+  Guards guards;   // checked build only
 };
 
 // Fills `L`; returns false for arguments no call can accept.

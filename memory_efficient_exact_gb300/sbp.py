@@ -15,11 +15,16 @@ import re
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libsbp.so")
+# SBP_LIBRARY_VARIANT selects a build of the same sources: "" (default), "checked" (guard
+# zones around workspace regions) or "nvtx" (NVTX ranges); see _build.py
+VARIANT = os.environ.get("SBP_LIBRARY_VARIANT", "")
+if VARIANT not in ("", "checked", "nvtx"):
+    raise ImportError(f"SBP_LIBRARY_VARIANT={VARIANT!r}: one of '', 'checked', 'nvtx'")
+LIB_PATH = os.path.join(_HERE, f"libsbp_{VARIANT}.so" if VARIANT else "libsbp.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "sbp.h")
 
 (OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_LABEL_RANGE, ERR_TIMEOUT, ERR_CUDA, ERR_UNSUPPORTED,
- ERR_SCRATCH_LIMIT) = range(9)
+ ERR_SCRATCH_LIMIT, ERR_WORKSPACE_OVERRUN) = range(10)
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 BF16, FP32 = 0, 1
 MODE_SFT, MODE_GRPO, MODE_DPO1, MODE_DPO2 = 0, 1, 2, 3

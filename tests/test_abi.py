@@ -158,6 +158,33 @@ def test_host_stream_argument_errors(sbp):
     assert call(wsb=sbp.workspace_bytes(16, 64, 128, 8, sbp.BF16, sbp.MODE_SFT)) == sbp.ERR_WORKSPACE
 
 
+def test_checked_and_nvtx_variants(sbp):
+    # the checked build (guard zones after every workspace region) and the NVTX build of the
+    # same sources: both export every header function; the checked build's workspace is
+    # larger by 256 bytes per region, the others' layouts are the release one
+    from memory_efficient_exact_gb300 import _build
+    names = sbp.header_functions()
+    libs = {}
+    for v in ("checked", "nvtx"):
+        path = _build.build_library(variant=v)
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+        exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+        assert not [n for n in names if n not in exported], v
+        lib = ctypes.CDLL(path)
+        lib.sbp_lmhead_workspace_bytes.restype = ctypes.c_size_t
+        lib.sbp_lmhead_workspace_bytes.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int] * 2
+        lib.sbp_status_string.restype = ctypes.c_char_p
+        lib.sbp_status_string.argtypes = [ctypes.c_int]
+        libs[v] = lib
+    args = (16384, 4096, 151936, 4096, sbp.BF16, sbp.MODE_SFT)
+    base = sbp.workspace_bytes(*args)
+    assert libs["nvtx"].sbp_lmhead_workspace_bytes(*args) == base
+    extra = libs["checked"].sbp_lmhead_workspace_bytes(*args) - base
+    assert extra > 0 and extra % 256 == 0 and extra <= 24 * 256
+    assert libs["checked"].sbp_status_string(sbp.ERR_WORKSPACE_OVERRUN) == b"SBP_ERR_WORKSPACE_OVERRUN"
+    assert sbp.status_string(sbp.ERR_WORKSPACE_OVERRUN) == "SBP_ERR_WORKSPACE_OVERRUN"
+
+
 def test_product_path_never_imports_the_oracle():
     pkg = os.path.join(ROOT, "memory_efficient_exact_gb300")
     for dp, _, fs in os.walk(pkg):
