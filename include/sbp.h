@@ -37,9 +37,11 @@
  * Errors: the return value is an sbp_status.  Argument errors are found on the host
  *   and returned before anything is enqueued (outputs untouched).  Errors only the
  *   device can see (a label outside [0, V) other than ignore_index; a pipeline wait
- *   that ran past its time limit) are written to *dev_status (device int32, zeroed by
- *   the call at enqueue); read it after synchronising.  After a device error the
- *   outputs are undefined.  No call traps the device.
+ *   that ran past its time limit; in the checked build, libsbp_checked.so, a write into
+ *   one of the guard zones it places after every workspace region) are written to
+ *   *dev_status (device int32, zeroed by the call at enqueue); read it after
+ *   synchronising.  After a device error the outputs are undefined.  No call traps the
+ *   device.  The checked build's workspace queries include its guard zones.
  * Reductions: the mean denominators are over the whole call, never per chunk.
  *   N = number of tokens with labels[t] != ignore_index.  When N = 0 the loss is 0
  *   and the gradients are 0.
