@@ -455,6 +455,10 @@ def run_mlp_bench(args):
         w["chunk"] = args.chunk
     if args.tokens:
         w["T"] = args.tokens
+    if args.d:
+        w["d"] = args.d
+    if args.f:
+        w["f"] = args.f
     T, d, f, chunk = w["T"], w["d"], w["f"], w["chunk"]
     w["workload"] = f"swiglu_mlp_bwd_bf16_T{T}_d{d}_f{f}_chunk{chunk}"
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -512,7 +516,8 @@ def run_mlp_bench(args):
         cpu = {"value": Ts / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"first {Ts} tokens (full d={d}, f={f}), float64 numpy/BLAS, one run"}
     line = {
-        "metric": MLP_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "metric": MLP_METRIC if (d, f) == (4096, 12288) else f"mlp sublayer bwd tokens/s (SwiGLU, d={d}, f={f})",
+        "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w["workload"], "T": T, "d": d, "f": f, "chunk": chunk},
@@ -573,6 +578,8 @@ def run_attn_bench(args):
         w["chunk"] = args.chunk
     if args.tokens:
         w["T"] = args.tokens
+    if args.heads:
+        w["H"] = args.heads
     if args.hd:
         w["hd"] = args.hd
     H, T, hd, chunk = w["H"], w["T"], w["hd"], w["chunk"]
@@ -697,7 +704,9 @@ def main(argv=None):
                     help="--sublayer attn: key / value heads (grouped-query attention; default = query heads)")
     ap.add_argument("--lean", action="store_true",
                     help="LM head: the smallest workspace (one chunk buffer, gradient as its own pass)")
-    ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps)")
+    ap.add_argument("--d", type=int, default=None, help="override the hidden size (sweeps; --sublayer mlp too)")
+    ap.add_argument("--f", type=int, default=None, help="--sublayer mlp: the intermediate size")
+    ap.add_argument("--heads", type=int, default=None, help="--sublayer attn: query heads")
     ap.add_argument("--sublayer", choices=["lmhead", "mlp", "attn"], default="lmhead",
                     help="mlp / attn: the chunked SwiGLU-MLP or causal-attention backward (own JSON line)")
     ap.add_argument("--objective", choices=["sft", "grpo", "dpo"], default="sft",

@@ -65,10 +65,11 @@ def test_attention_backward_parity(sbp, H, T, hd, chunk):
 
 
 # grouped-query attention (key / value heads shared by H / Hkv query heads, the Qwen3
-# layout): head dimension 128, groups of 2, 3 and 4, one shared head (multi-query), ragged
-# chunks, and more units than SM pairs
+# layout): head dimension 128, groups of 2 to 8 (8: the Qwen3-32B ratio, 5: Qwen3-14B),
+# one shared head (multi-query), ragged chunks, and more units than SM pairs
 @pytest.mark.parametrize("H,Hkv,T,chunk", [(8, 2, 640, 256), (4, 1, 513, 200), (6, 3, 96, 40),
-                                           (48, 8, 1024, 512), (2, 1, 1, 1)])
+                                           (48, 8, 1024, 512), (2, 1, 1, 1),
+                                           (16, 2, 520, 200), (10, 2, 384, 384)])
 def test_attention_gqa_parity(sbp, H, Hkv, T, chunk):
     hd = 128
     Q, K, V, O, dO, lse, scale = make(H, T, hd, seed=H * 100 + Hkv * 10 + T, Hkv=Hkv)
