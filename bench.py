@@ -687,6 +687,72 @@ def run_attn_bench(args):
     return 0
 
 
+# ------------------------------------------------------- timing comparator (opt-in only)
+
+def run_torch_comparator(args):
+    """The same chunked SFT LM head written as plain eager PyTorch (cuBLAS bf16 GEMMs,
+    fp32 softmax), timed on the same workload: what the hand-written kernels buy over an
+    idiomatic implementation of the method.  A timing comparison only: nothing of the
+    library's path runs here, and nothing of this runs in the library."""
+    import torch
+    w = WORKLOAD
+    T, d, V, chunk = w["T"], w["d"], w["V"], w["chunk"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    H, W, y = make_inputs(0)
+    Ht = torch.from_numpy(H).to(dev).to(torch.bfloat16)
+    Wt = torch.from_numpy(W).to(dev).to(torch.bfloat16)
+    yt = torch.from_numpy(y).to(dev).long()
+    dH = torch.empty_like(Ht)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        valid_all = yt != -100
+        n = valid_all.sum().clamp_min(1).float()
+        dW.zero_()
+        loss = torch.zeros((), dtype=torch.float32, device=dev)
+        for c0 in range(0, T, chunk):
+            h, yc, vc = Ht[c0:c0 + chunk], yt[c0:c0 + chunk], valid_all[c0:c0 + chunk]
+            z = (h @ Wt.T).float()
+            lse = torch.logsumexp(z, dim=1)
+            logp = z.gather(1, yc.clamp_min(0)[:, None])[:, 0] - lse
+            loss -= (logp * vc).sum() / n
+            g = torch.exp(z - lse[:, None])
+            g[torch.arange(g.shape[0], device=dev), yc.clamp_min(0)] -= 1.0
+            g *= (vc.float() / n)[:, None]
+            gb = g.to(torch.bfloat16)
+            dH[c0:c0 + chunk] = gb @ Wt
+            dW.add_((gb.T @ h).float())
+        return loss
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_id_for(torch, dev))
+    time.sleep(0.3)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    peaks, src = load_peaks()
+    value = T * args.steps / (ms / 1000.0)
+    line = {
+        "comparator": "eager PyTorch (cuBLAS bf16 GEMMs, fp32 softmax), same chunking",
+        "metric": METRIC if (d, V) == (4096, 151936) else f"lm_head fwd+bwd tokens/s (sft, d={d}, V={V})",
+        "value": value, "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "pct_bf16_peak": 100.0 * 6.0 * d * V * value / 1e12 / peaks["bf16_tflops"], "peak_source": src,
+        "config": {k: w[k] for k in ("workload", "T", "d", "V", "chunk")},
+        "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -694,6 +760,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--comparator", choices=["torch"], default=None,
+                    help="time the same chunked LM head in eager PyTorch instead (a comparison line only)")
     ap.add_argument("--workload", choices=["main", "profile"] + sorted(SWEEP_WORKLOADS), default="main",
                     help="profile: a small case of the same kernels for ncu captures; "
                          "sft_T8192_d2560 / sft_T65536_d5120: the chunk-sweep workloads (with --chunk)")
@@ -735,6 +803,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.comparator == "torch":
+        return run_torch_comparator(args)
     if args.sublayer == "mlp":
         return run_mlp_bench(args)
     if args.sublayer == "attn":
