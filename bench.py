@@ -14,6 +14,16 @@ N > 1 runs under torchrun, one rank per GPU; every rank processes its own batch
 (weak scaling, no collective on the data path); the timing is the max over ranks.
 ``--impl reference`` times the float64 CPU oracle on a bounded sample of the same
 workload instead (rank 0 only).
+
+Other lines (each its own JSON line; not the driver's):
+  --objective grpo|dpo          the other objectives (8 x 2048 / 8 x 4096 tokens)
+  --workload sft_T8192_d2560|sft_T65536_d5120 [--chunk C]   the chunk-sweep workloads
+  --workload profile            a small case of the same kernels for ncu captures
+  --lean                        the one-buffer workspace schedule
+  --sublayer mlp [--d D --f F]  the chunked SwiGLU-MLP backward
+  --sublayer attn [--heads H --kv-heads K --hd 64..256 --tokens T --chunk C]
+                                the chunked causal-attention backward
+  --comparator torch            the same chunked LM head in eager PyTorch (timing only)
 """
 from __future__ import annotations
 
