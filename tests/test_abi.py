@@ -7,6 +7,7 @@ is enqueued) must behave as the header states.
 import ctypes
 import os
 import subprocess
+import sys
 
 import pytest
 
@@ -192,3 +193,24 @@ def test_product_path_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".h", ".cuh")):
                 src = open(os.path.join(dp, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_binding_fails_loudly_without_its_library(tmp_path):
+    # an unknown variant, and a package copy whose library was never built, both raise on
+    # import: there is no other implementation to fall back to
+    env = dict(os.environ, SBP_LIBRARY_VARIANT="bogus")
+    code = f"import sys; sys.path.insert(0, {ROOT!r}); import memory_efficient_exact_gb300.sbp"
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert r.returncode != 0 and "SBP_LIBRARY_VARIANT" in r.stderr
+    import shutil
+    pkg = tmp_path / "memory_efficient_exact_gb300"
+    pkg.mkdir()
+    for f in ("__init__.py", "sbp.py"):
+        src = os.path.join(ROOT, "memory_efficient_exact_gb300", f)
+        if os.path.exists(src):
+            shutil.copy(src, pkg / f)
+    env = dict(os.environ)
+    env.pop("SBP_LIBRARY_VARIANT", None)
+    code = f"import sys; sys.path.insert(0, {str(tmp_path)!r}); import memory_efficient_exact_gb300.sbp"
+    r = subprocess.run([sys.executable, "-c", code], cwd=str(tmp_path), env=env, capture_output=True, text=True)
+    assert r.returncode != 0 and "is missing" in r.stderr
