@@ -173,3 +173,32 @@ def test_gqa_finite_differences():
             X[i] = old
             G[i] = (lp - lm) / 2e-6
         np.testing.assert_allclose(b[key], G, rtol=1e-6, atol=1e-8)
+
+
+# randomised shapes: query / key-value head counts (grouped-query included), lengths,
+# widths, scales and chunks, each against PyTorch's SDPA autograd in float64 and against
+# the chunked decomposition
+@pytest.mark.parametrize("seed", range(16))
+def test_random_shapes_against_sdpa_and_chunking(seed):
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(1000 + seed)
+    Hkv = int(g.integers(1, 4))
+    H = Hkv * int(g.integers(1, 4))
+    T = int(g.integers(1, 12))
+    hd = int(g.integers(1, 7))
+    s = float(g.uniform(0.2, 1.0))
+    chunk = int(g.integers(1, T + 2))
+    Q, dO = g.standard_normal((H, T, hd)), g.standard_normal((H, T, hd))
+    K, V = g.standard_normal((Hkv, T, hd)), g.standard_normal((Hkv, T, hd))
+    f = A.forward(Q, K, V, s)
+    b = A.backward(Q, K, V, f["O"], dO, f["lse"], s)
+    q, k, v = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True, scale=s,
+                                                         enable_gqa=True)[0]
+    o.backward(torch.tensor(dO))
+    np.testing.assert_allclose(f["O"], o.detach().numpy(), rtol=1e-11, atol=1e-12)
+    for t, key in ((q, "dQ"), (k, "dK"), (v, "dV")):
+        np.testing.assert_allclose(b[key], t.grad.numpy(), rtol=1e-10, atol=1e-11)
+    c = A.backward_chunked(Q, K, V, f["O"], dO, f["lse"], s, chunk)
+    for key in ("dQ", "dK", "dV"):
+        np.testing.assert_allclose(c[key], b[key], rtol=1e-12, atol=1e-12)

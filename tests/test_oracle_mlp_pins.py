@@ -82,3 +82,25 @@ def _fd_dx(x, Wg, Wu, Wd, dY):
             x[i, j] = old
             G[i, j] = (lp - lm) / 2e-6
     np.testing.assert_allclose(b["dx"], G, rtol=1e-6, atol=1e-8)
+
+
+# randomised shapes and weight scales against PyTorch autograd in float64, and the row
+# decomposition at a random chunk
+@pytest.mark.parametrize("seed", range(16))
+def test_random_shapes_against_autograd_and_chunking(seed):
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(2000 + seed)
+    T, d, f = int(g.integers(1, 10)), int(g.integers(1, 7)), int(g.integers(1, 9))
+    sc = float(g.uniform(0.2, 1.5))
+    x, dY = g.standard_normal((T, d)), g.standard_normal((T, d))
+    Wg, Wu, Wd = sc * g.standard_normal((f, d)), sc * g.standard_normal((f, d)), sc * g.standard_normal((d, f))
+    b = M.backward(x, Wg, Wu, Wd, dY)
+    xt, gt, ut, dt = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (x, Wg, Wu, Wd))
+    y = (torch.nn.functional.silu(xt @ gt.T) * (xt @ ut.T)) @ dt.T
+    y.backward(torch.tensor(dY))
+    np.testing.assert_allclose(b["y"], y.detach().numpy(), rtol=1e-12, atol=1e-12)
+    for t, key in ((xt, "dx"), (gt, "dWg"), (ut, "dWu"), (dt, "dWd")):
+        np.testing.assert_allclose(b[key], t.grad.numpy(), rtol=1e-11, atol=1e-11)
+    c = M.backward_chunked(x, Wg, Wu, Wd, dY, int(g.integers(1, T + 2)))
+    for key in ("dx", "dWg", "dWu", "dWd"):
+        np.testing.assert_allclose(c[key], b[key], rtol=1e-12, atol=1e-12)
