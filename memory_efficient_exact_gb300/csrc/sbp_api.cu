@@ -1151,16 +1151,17 @@ int run_attn_fused(const void* Q, const void* K, const void* Vv, const void* O, 
     SBP_CUDA(cudaStreamWaitEvent(ss->s, ss->fork, 0));
     sq = ss->s;
   }
-  // One k_attn_kv launch may cover a run of consecutive chunks (up to kKvSpan queries):
-  // nothing of size (queries x keys) is stored on this path, so the span changes no
-  // memory, and a unit (one key / value head, 256 keys) then walks more query blocks for
-  // each K / V load and dK / dV write-back.  A run is taken only if its launch still has
-  // at least 4 units per SM pair, since longer units balance worse (measured: merging
-  // 4 chunks of 1024 gave +2% with 32 key / value heads, -5% with 8).  k_attn_q keeps the
-  // caller's chunks.  Both schedules are fixed by the arguments, so the results stay
-  // bitwise repeatable.
+  // With one key / value head per query head, one k_attn_kv launch may cover a run of
+  // consecutive chunks (up to kKvSpan queries): nothing of size (queries x keys) is stored
+  // on this path, so the span changes no memory, and a unit (one head, 256 keys) then
+  // walks more query blocks for each K / V load and dK / dV write-back.  A run is taken
+  // only if its launch still has at least 4 units per SM pair.  Measured: merging 4
+  // chunks of 1024 gave +2% with 32 heads at T = 8192; with grouped heads (units 4 times
+  // longer and fewer) it lost 5% at T = 8192 and 3.5% at T = 32768, so grouped heads keep
+  // one launch per chunk.  k_attn_q keeps the caller's chunks.  Both schedules are fixed
+  // by the arguments, so the results stay bitwise repeatable.
   constexpr int64_t kKvSpan = 4096;
-  const int64_t kv_max = std::max<int64_t>(1, kKvSpan / L.chunk);
+  const int64_t kv_max = Hkv == H ? std::max<int64_t>(1, kKvSpan / L.chunk) : 1;
   const int64_t min_units = 4 * std::max(1, num_sms() / 2);
   auto kv_units = [&](int64_t c1) { return ((c1 + 255) / 256) * Hkv; };
   int64_t kv_next = 0;   // first chunk no k_attn_kv launch has covered yet
