@@ -214,3 +214,23 @@ def test_binding_fails_loudly_without_its_library(tmp_path):
     code = f"import sys; sys.path.insert(0, {str(tmp_path)!r}); import memory_efficient_exact_gb300.sbp"
     r = subprocess.run([sys.executable, "-c", code], cwd=str(tmp_path), env=env, capture_output=True, text=True)
     assert r.returncode != 0 and "is missing" in r.stderr
+
+
+def test_header_is_plain_c(sbp, tmp_path):
+    # the boundary is a C ABI: the header compiles as C99 (and as C++) on its own, and every
+    # function it declares can be referenced from C
+    import shutil
+    names = sbp.header_functions()
+    src = tmp_path / "uses_every_function.c"
+    body = "\n".join(f"    (any_fn){n}," for n in names)
+    src.write_text('#include "sbp.h"\n#include <stddef.h>\n'
+                   "typedef void (*any_fn)(void);\n"
+                   f"static const any_fn table[] = {{\n{body}\n}};\n"
+                   "int main(void) { return table[0] == NULL; }\n")
+    inc = os.path.join(ROOT, "include")
+    for cc, extra in (("gcc", ["-std=c99", "-x", "c"]), ("g++", ["-std=c++17", "-x", "c++"])):
+        if not shutil.which(cc):
+            pytest.skip(f"{cc} not available")
+        r = subprocess.run([cc, *extra, "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc, "-c", str(src),
+                            "-o", str(tmp_path / f"t_{cc}.o")], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
