@@ -165,7 +165,7 @@ def make_inputs(rank: int, T: int | None = None):
     w = WORKLOAD
     T = w["T"] if T is None else T
     H, W = I.make_hw(T, w["d"], w["V"], w["seed"] + rank, w["dtype"])
-    y = I.make_labels(T, w["V"], w["seed"] + rank, w["mask"], w["frac"], w.get("n", 0))
+    y = I.make_labels(T, w["V"], w["seed"] + rank, w["mask"], w["frac"], w.get("n", 0), w.get("seq_len", 0))
     return H, W, y
 
 
@@ -243,20 +243,28 @@ def run_ours(args):
 
     objective = w.get("objective", "sft")
     if objective == "grpo":
-        # per-response advantages; old log-probs near the workload's typical label
-        # log-prob (-log V) plus noise: their values steer only the clip branches
+        # per-response advantages A ~ N(0, 1); old log-probs = the exact current label
+        # log-probs plus N(0, 0.1^2) noise, fixed at generation: computed once here, before
+        # the timed region, by one forward-only library call (the first DPO pass over a
+        # single sequence returns every token's log-prob and forms no gradient)
         from memory_efficient_exact_gb300 import inputs as I
         n_resp = max(1, T // 2048)
         At = torch.from_numpy(I.make_advantages(n_resp, (T + n_resp - 1) // n_resp, w["seed"])[:T]).to(dev)
-        lpo = torch.from_numpy((-12.8 + I.make_logp_noise(T, w["seed"])).astype("float32")).to(dev)
         ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_GRPO, dev, lean=lean)
+        ws1 = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_DPO1, dev)
+        one = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        cur = sbp.dpo_pass1(Ht, Wt, yt, one, chunk, workspace=ws1, status=st, logp=True, stream=stream)
+        torch.cuda.synchronize(dev)
+        sbp.check_status(st, "old log-probs")
+        lpo = (cur["logp"].double() + torch.from_numpy(I.make_logp_noise(T, w["seed"])).to(dev)).float()
+        del ws1, cur
 
         def step():
             return sbp.grpo(Ht, Wt, yt, At, lpo, chunk, dH=dH, dW=dW, workspace=ws, status=st, logp=False,
                             stream=stream)
     elif objective == "dpo":
         from memory_efficient_exact_gb300 import inputs as I
-        n_seq = max(2, T // 4096)
+        n_seq = max(2, T // w.get("seq_len", 4096))
         cu = torch.from_numpy(I.cu_seqlens(n_seq, T // n_seq)).to(dev)
         sref = torch.from_numpy(I.make_ref_seq_logp(n_seq, w["seed"])).to(dev)
         ws = sbp.make_workspace(T, d, V, chunk, sbp.BF16, sbp.MODE_DPO2, dev, lean=lean)
@@ -300,7 +308,9 @@ def run_ours(args):
     prof = sbp.profile_read()
     sbp.check_status(st, "timed region")
     ms_local = e0.elapsed_time(e1)
-    peak_mem = torch.cuda.max_memory_allocated(dev)
+    # torch's peak plus the library's one static device array (the scratch of the
+    # allocation-free entry point), which every GPU that loads the library holds
+    peak_mem = torch.cuda.max_memory_allocated(dev) + sbp.NOALLOC_SCRATCH_BYTES
     loss = float(out["loss"].item())
 
     tokens_all, ms = aggregate(torch, dist, float(T * args.steps), ms_local, dev)
@@ -546,7 +556,7 @@ def run_mlp_bench(args):
         "executed_tflops": executed * value / 1e12,
         "pct_bf16_peak_executed": 100.0 * executed * value / 1e12 / peaks["bf16_tflops"],
         "pct_bf16_peak_credited_12dF": 100.0 * 12.0 * d * f * value / 1e12 / peaks["bf16_tflops"],
-        "peak_source": src, "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+        "peak_source": src, "peak_mem_gb": (torch.cuda.max_memory_allocated(dev) + sbp.NOALLOC_SCRATCH_BYTES) / 1e9,
         "unchunked_activations_gb": 3 * T * f * 2 / 1e9,
         "gpu_launches": launches * args.steps, "clocks": clk, "cpu_baseline": cpu,
     }
@@ -685,7 +695,7 @@ def run_attn_bench(args):
                                "tflops": 2 * gemms[1] * hd * H * rowkeys * args.steps / (bw_ms / 1000.0) / 1e12
                                if bw_n else None},
                     "other": {"ms": prof["other"][0], "launches": prof["other"][1]}},
-        "peak_source": src, "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+        "peak_source": src, "peak_mem_gb": (torch.cuda.max_memory_allocated(dev) + sbp.NOALLOC_SCRATCH_BYTES) / 1e9,
         "unchunked_scores_gb": H * T * T * 2 * 2 / 1e9,
         "gpu_launches": launches * args.steps, "clocks": clk,
     }
@@ -800,8 +810,9 @@ def main(argv=None):
         if args.chunk is None:
             args.chunk = WORKLOAD["chunk"]
     WORKLOAD["objective"] = args.objective
-    if args.objective == "dpo" and args.tokens is None and args.workload == "main":
-        WORKLOAD["T"] = 32768
+    if args.objective == "dpo" and args.workload == "main":
+        # the DPO input recipe: 8 sequences of 4096 tokens, the first 1024 of each masked
+        WORKLOAD.update(T=32768, seed=1003, mask="seqhead", n=1024, seq_len=4096, frac=0.0)
     for key, val in (("chunk", args.chunk), ("T", args.tokens), ("d", args.d)):
         if val is not None:
             WORKLOAD[key] = val

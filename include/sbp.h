@@ -253,9 +253,13 @@ int sbp_attn_causal_backward_gqa(const void* Q, const void* K, const void* V, co
  * allocator.  They pass only inputs and outputs, and the call works in one statically
  * sized device array of SBP_NOALLOC_SCRATCH_BYTES (64 MiB) that the library defines;
  * every GPU that loads the library holds that array until the process exits.
- * Sizes whose workspace (sbp_lmhead_workspace_bytes with SBP_MODE_SFT) exceeds it are
- * rejected on the host with SBP_ERR_SCRATCH_LIMIT before anything is enqueued; with
- * V = 151936 and d = 4096, chunks up to about 96 rows fit.  The first call on a device
+ * The call runs the one-buffer schedule, so the size it checks is the one-buffer
+ * workspace, sbp_lmhead_workspace_bytes_lean(T, d, V, chunk, dtype, SBP_MODE_SFT):
+ * sizes for which that exceeds the array are rejected on the host with
+ * SBP_ERR_SCRATCH_LIMIT before anything is enqueued.  With V = 151936 and d = 4096 on a
+ * 152-SM GB300, chunks up to about 130 rows fit (the figure moves slightly with T and
+ * the SM count, through the per-token regions and the dH split count).  The results are
+ * those of sbp_lmhead_sft given a one-buffer workspace, bit for bit.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  All calls share the one
  * array: calls that overlap on the GPU (other streams, other host threads) race and

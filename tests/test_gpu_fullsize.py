@@ -5,7 +5,8 @@ the same definitions row by row: every row's lse / logp (all rows: the loss and 
 DPO sums need them), dH on seeded sampled rows, dW on seeded sampled vocabulary rows
 (which needs every row's lse).  The 65536-token workload follows its own recipe:
 per-token loss and dH on sampled rows of the full run, and the full dW of the
-4096-token prefix sub-problem.
+4096-token prefix sub-problem; the GRPO and DPO workloads add the same kind of
+sub-problem check (full dH and dW of 4096 of their tokens, unchunked in the oracle).
 """
 import numpy as np
 import pytest
@@ -83,8 +84,13 @@ def test_sft_T8192_d2560(sbp, c2, chunk):
     check_sampled(H, W, y, w, c2["lse"], out, rows, vocab_sample(y, W.shape[0], chunk), f" chunk={chunk}")
 
 
-def test_grpo_8x2048_d4096(sbp):
-    x = I.make_workload("grpo_bf16_8x2048_d4096_V151936")
+@pytest.fixture(scope="module")
+def c3():
+    return I.make_workload("grpo_bf16_8x2048_d4096_V151936")
+
+
+def test_grpo_8x2048_d4096(sbp, c3):
+    x = c3
     H, W, y = x["H"], x["W"], x["labels"]
     lse, logp = O.rows_lse_logp(H, W, y, None, IGN)
     valid = y != IGN
@@ -102,8 +108,35 @@ def test_grpo_8x2048_d4096(sbp):
     check_sampled(H, W, y, gar / N, lse, out, I.sample_rows(len(y), 256, 1002), vocab_sample(y, W.shape[0], 3))
 
 
-def test_dpo_8x4096_d4096(sbp):
-    x = I.make_workload("dpo_bf16_8x4096_d4096_V151936")
+def test_grpo_8x2048_d4096_prefix_full_dW(sbp, c3):
+    """The first two responses (4096 tokens) as a problem of their own, in the bench's
+    chunking (two chunks of 2048): full dH and full dW against the unchunked oracle."""
+    Tp = 4096
+    H, W = np.ascontiguousarray(c3["H"][:Tp]), c3["W"]
+    y = np.ascontiguousarray(c3["labels"][:Tp])
+    _, logp = O.rows_lse_logp(H, W, y, None, IGN)
+    lpo = (logp + c3["logp_noise"][:Tp]).astype(np.float32)
+    A = np.ascontiguousarray(c3["advantages"][:Tp]).astype(np.float32)
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    out = sbp.grpo(Ht, Wt, yt, torch.from_numpy(A).cuda(), torch.from_numpy(lpo).cuda(), 2048)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.grpo(H, W, y, A.astype(np.float64), lpo.astype(np.float64), IGN)
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= BF["loss"]
+    dH = out["dH"].float().cpu().numpy()
+    assert rel_fro(dH, ref["dH"]) <= BF["grad"]
+    assert rel_fro(out["dW"].cpu().numpy(), ref["dW"]) <= BF["grad"]
+    assert np.all(dH[y == IGN] == 0.0)
+
+
+@pytest.fixture(scope="module")
+def c4():
+    return I.make_workload("dpo_bf16_8x4096_d4096_V151936")
+
+
+def test_dpo_8x4096_d4096(sbp, c4):
+    x = c4
     H, W, y, cu, Sref = x["H"], x["W"], x["labels"], x["cu_seqlens"], x["ref_seq_logp"]
     lse, logp = O.rows_lse_logp(H, W, y, None, IGN)
     valid = y != IGN
@@ -122,6 +155,35 @@ def test_dpo_8x4096_d4096(sbp):
     assert np.max(np.abs(Sg - S) / np.abs(S)) <= BF["seq"]
     assert rel(p2["loss"].item(), ref_loss) <= BF["loss"]
     check_sampled(H, W, y, w, lse, p2, I.sample_rows(len(y), 256, 1003), vocab_sample(y, W.shape[0], 4))
+
+
+def test_dpo_8x4096_d4096_prefix_full_dW(sbp, c4):
+    """One preference pair as a problem of its own: the first 2048 tokens of the chosen
+    sequence 0 and of its rejected partner, sequence 4 (each with its 1024-token head
+    masked, as in the workload), with their reference sums.  Pass 1's sums go through
+    pass 2 on the device, in the bench's chunking; full dH and full dW against the
+    unchunked oracle."""
+    L, Lw = 2048, 4096
+    rows = np.concatenate([np.arange(0, L), np.arange(4 * Lw, 4 * Lw + L)])
+    H, W = np.ascontiguousarray(c4["H"][rows]), c4["W"]
+    y = np.ascontiguousarray(c4["labels"][rows])
+    cu = np.array([0, L, 2 * L], dtype=np.int32)
+    Sref = np.ascontiguousarray(c4["ref_seq_logp"][[0, 4]])
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    cut = torch.from_numpy(cu).cuda()
+    p1 = sbp.dpo_pass1(Ht, Wt, yt, cut, 2048)
+    p2 = sbp.dpo_pass2(Ht, Wt, yt, cut, p1["seq_logp"], torch.from_numpy(Sref).cuda(), 0.1, 2048)
+    torch.cuda.synchronize()
+    sbp.check_status(p1["status"])
+    sbp.check_status(p2["status"])
+    ref = O.dpo(H, W, y, cu, Sref, 0.1, IGN)
+    Sg = p1["seq_logp"].cpu().numpy()
+    assert np.max(np.abs(Sg - ref["seq_logp"]) / np.abs(ref["seq_logp"])) <= BF["seq"]
+    assert rel(p2["loss"].item(), ref["loss"]) <= BF["loss"]
+    dH = p2["dH"].float().cpu().numpy()
+    assert rel_fro(dH, ref["dH"]) <= BF["grad"]
+    assert rel_fro(p2["dW"].cpu().numpy(), ref["dW"]) <= BF["grad"]
+    assert np.all(dH[y == IGN] == 0.0)
 
 
 @pytest.fixture(scope="module")
@@ -158,8 +220,11 @@ def test_sft_T65536_d5120_sampled(sbp, c5, chunk):
     rows, logp_s = c5["rows"], c5["logp_s"]
     lp = out["logp"].cpu().numpy()
     assert np.max(np.abs(lp[rows] - logp_s)) <= BF["logp"] * np.abs(logp_s).max()
-    # the loss is the mean of the per-token terms (a property at any size)
+    # the loss is the mean of the per-token terms (a property at any size) ...
     assert rel(out["loss"].item(), -lp[valid].astype(np.float64).sum() / N) <= 1e-5
+    # ... and over the sampled rows that mean agrees with the oracle's
+    vs = valid[rows]
+    assert rel(-lp[rows][vs].astype(np.float64).mean(), -logp_s[vs].mean()) <= BF["loss"]
     got = out["dH"][torch.from_numpy(c5["sub"]).cuda()].float().cpu().numpy()
     assert rel_fro(got, c5["ref_dh"]) <= BF["grad"]
     assert torch.count_nonzero(out["dH"][torch.from_numpy(~valid).cuda()]).item() == 0
