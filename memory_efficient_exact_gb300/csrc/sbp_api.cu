@@ -206,10 +206,18 @@ __device__ __forceinline__ int seq_of(const int32_t* cu, int n_seq, int64_t t) {
   return lo;
 }
 
-// One warp per row: lse = M + log sum_i s_i exp(m_i - M) over the row's tile partials,
-// logp = z_y - lse, then the objective's weight w and loss term.  The tile maxima are
-// replaced in place by the gradient scales w exp(m_i - lse), so that the gradient
-// kernel needs one multiply per element: G = e * scale - w [v = y].
+// One warp per row over the row's tile partials (m_i, r_i), where r_i = sum of
+// exp(z - m_i) over the tile's columns less the one at the tile's maximum (whose term is
+// exactly 1).  With M = max_i m_i, the sum of exp(z - M) over the whole row is 1 + R,
+//   R = sum_{i: m_i < M} (1 + r_i) exp(m_i - M) + sum_{i: m_i = M} r_i + (#{i: m_i = M} - 1),
+// a sum of non-negative terms, so lse = M + log1p(R) and logp = (z_y - M) - log1p(R) keep
+// their relative precision when the label holds almost all the probability mass (R -> 0,
+// the confident-token regime), where 1 + R itself would round to 1.  Then the
+// objective's weight w and loss term.  The tile maxima are replaced in place by the
+// gradient scales w exp(m_i - lse), so that the gradient kernel needs one multiply per
+// element, G = e * scale; the label's own entry, w (p_y - 1) = w expm1(logp), is written
+// into the second field of the label's tile partial, so that it does not come from the
+// cancelling difference e_y * scale - w.
 template <int MODE>
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
   const int lane = threadIdx.x % 32;
@@ -219,16 +227,21 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
   float m = -FLT_MAX;
   for (int64_t i = lane; i < a.ntiles; i += 32) m = fmaxf(m, p[i].x);
   m = warp_max(m);
-  float s = 0.f;
+  float rest = 0.f, ties = 0.f;
   for (int64_t i = lane; i < a.ntiles; i += 32) {
     const float2 q = p[i];
-    s += q.y * expf(q.x - m);
+    if (q.x == m) {
+      rest += q.y;
+      ties += 1.f;
+    } else {
+      rest += (1.f + q.y) * expf(q.x - m);
+    }
   }
-  s = warp_sum(s);
-  const float lse = m + logf(s);
+  rest = warp_sum(rest) + (warp_sum(ties) - 1.f);
+  const float l1 = log1pf(rest);
   const int32_t y = a.labels[row];
   const bool valid = y != a.ign && y >= 0 && (int64_t)y < a.V;
-  const float logp = valid ? a.zy[row] - lse : 0.f;
+  const float logp = valid ? (a.zy[row] - m) - l1 : 0.f;
   const long long N = *a.nvalid;
   const float invN = N > 0 ? (float)(1.0 / (double)N) : 0.f;
   float w = 0.f, tl = 0.f;
@@ -262,7 +275,9 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
     const int sq = valid ? seq_of(a.cu, a.n_seq, t) : -1;
     if (sq >= 0) w = a.seqw[sq];
   }
-  for (int64_t i = lane; i < a.ntiles; i += 32) p[i].x = w * expf(p[i].x - lse);
+  const int64_t ty = valid ? (int64_t)y / kStatW : -1;
+  const float gy = w * expm1f(logp);
+  for (int64_t i = lane; i < a.ntiles; i += 32) p[i] = make_float2(w * expf((p[i].x - m) - l1), i == ty ? gy : 0.f);
   if (lane == 0) {
     a.w_row[row] = w;
     a.logp[t] = logp;
@@ -300,7 +315,8 @@ __device__ __forceinline__ void st1(__nv_bfloat16* p, float v) { *p = __float2bf
 __device__ __forceinline__ void st1(float* p, float v) { *p = v; }
 
 // Logit gradient of one chunk, in place over the chunk buffer:
-//   G[r, v] = e[r, v] * scale[r, tile(v)] - w_r [v = y_r]   (= w_r (softmax - onehot)).
+//   G[r, v] = e[r, v] * scale[r, tile(v)] for v != y_r, and w_r expm1(logp_r) at the
+//   label (both from the combine step), i.e. w_r (softmax - onehot).
 // TE -> TG: fp16 -> bf16 (tensor-core path) or fp32 -> fp32 (SIMT path).
 template <typename TE, typename TG>
 __global__ void __launch_bounds__(256) k_grad(void* buf, int64_t ld, int64_t V, const float2* __restrict__ part,
@@ -322,17 +338,15 @@ __global__ void __launch_bounds__(256) k_grad(void* buf, int64_t ld, int64_t V, 
         for (int i = 0; i < 8; ++i) f[i] = 0.f;
       } else {
         load8(e + v0, f);
-        const float s = sc[v0 / kStatW].x;
+        const float2 s = sc[v0 / kStatW];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] *= s;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (v0 + i == (int64_t)y) f[i] -= w;
+        for (int i = 0; i < 8; ++i) f[i] = v0 + i == (int64_t)y ? s.y : f[i] * s.x;
       }
       store8(g + v0, f);
     } else {
       for (int64_t v = v0; v < V; ++v) {
-        float x = w == 0.f ? 0.f : ld1(e + v) * sc[v / kStatW].x - (v == y ? w : 0.f);
+        const float2 s = sc[v / kStatW];
+        const float x = w == 0.f ? 0.f : (v == y ? s.y : ld1(e + v) * s.x);
         st1(g + v, x);
       }
     }

@@ -80,11 +80,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // One block of kStatW threads per (tile, row): the tile's max m, e = exp(z - m) written
-// over z, s = sum e, and the label's logit gathered when it falls in the tile.
+// over z, s = sum e less the maximum's own term 1, and the label's logit gathered when
+// it falls in the tile.
 __global__ void __launch_bounds__(kStatW) k_tile_stats_f32(float* __restrict__ E, int64_t lde, int64_t V,
                                                            int64_t ntiles, const int32_t* __restrict__ labels,
                                                            float2* __restrict__ part, float* __restrict__ zy) {
-  __shared__ float red[kStatW / 32];
+  __shared__ float red[kStatW / 32], cnt[kStatW / 32];
   const int64_t row = blockIdx.y, tile = blockIdx.x;
   const int64_t col = tile * kStatW + threadIdx.x;
   const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
@@ -99,14 +100,24 @@ __global__ void __launch_bounds__(kStatW) k_tile_stats_f32(float* __restrict__ E
   __syncthreads();
   const float x = col < V ? expf(z - m) : 0.f;
   if (col < V) e[col] = x;
-  float s = warp_sum(x);
-  if (lane == 0) red[wid] = s;
+  // the tile's sum less the term of one maximum (exactly 1); the other maxima count 1
+  const bool top = col < V && z == m;
+  float s = warp_sum(top ? 0.f : x);
+  float c = warp_sum(top ? 1.f : 0.f);
+  if (lane == 0) {
+    red[wid] = s;
+    cnt[wid] = c;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     s = 0.f;
+    c = -1.f;
 #pragma unroll
-    for (int i = 0; i < kStatW / 32; ++i) s += red[i];
-    part[row * ntiles + tile] = make_float2(m, s);
+    for (int i = 0; i < kStatW / 32; ++i) {
+      s += red[i];
+      c += cnt[i];
+    }
+    part[row * ntiles + tile] = make_float2(m, s + c);
   }
   if (col < V && labels[row] == (int32_t)col) zy[row] = z;
 }

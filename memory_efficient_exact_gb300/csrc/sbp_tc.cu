@@ -15,7 +15,8 @@
 //
 // k_fwd  : Z_c = H_c W^T  (A = H rows, B = W rows, both K-major), epilogue = row
 //          statistics per 128-column tile: max m, e = exp(z - m) stored as fp16,
-//          s = sum e, and the label logit z_y (the chunk forward of the StreamBP LM head).
+//          s = sum e less the maximum's own term 1, and the label logit z_y (the chunk
+//          forward of the StreamBP LM head).
 // k_bwd  : one dynamic queue of units of two kinds, dH first:
 //          dH_c = G_c W    (A = G rows, K-major; B = W, MN-major), split along V,
 //          dW  += G_c^T H_c (A = G columns, MN-major; B = H_c, MN-major).
@@ -42,7 +43,9 @@ struct FwdP {
   int32_t* status; uint64_t limit_ns;
   int stall;   // failure-detection test: the MMA thread first waits on a barrier nothing arrives on
   // The previous chunk's logit gradient, formed by the epilogue warps in the time they
-  // do not need for this chunk's tiles: G = e * scale - w [v = y], fp16 -> bf16 in place.
+  // do not need for this chunk's tiles: G = e * scale, and at the label the entry
+  // w expm1(logp) that the combine step left beside the label tile's scale; fp16 -> bf16
+  // in place.
   __half* gprev;              // nullptr: no previous chunk to convert
   const float2* part_prev;    // its tile scales
   const float* w_prev;        // its row weights
@@ -66,18 +69,18 @@ __device__ __forceinline__ void side_vector(const FwdP& p, int64_t r, int64_t v0
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
     if (w != 0.f) {
       const uint4 in = *reinterpret_cast<const uint4*>(e + v0);
-      const float s = p.part_prev[r * p.ntiles + v0 / kStatW].x;
+      const float2 s = p.part_prev[r * p.ntiles + v0 / kStatW];
       const __half2* hin = reinterpret_cast<const __half2*>(&in);
       float f[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 x = __half22float2(hin[i]);
-        f[2 * i] = x.x * s;
-        f[2 * i + 1] = x.y * s;
+        f[2 * i] = x.x * s.x;
+        f[2 * i + 1] = x.y * s.x;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (v0 + i == (int64_t)y) f[i] -= w;
+        if (v0 + i == (int64_t)y) f[i] = s.y;
       __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&out);
 #pragma unroll
       for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
@@ -85,8 +88,8 @@ __device__ __forceinline__ void side_vector(const FwdP& p, int64_t r, int64_t v0
     *reinterpret_cast<uint4*>(g + v0) = out;
   } else {
     for (int64_t v = v0; v < p.V; ++v) {
-      const float x = w == 0.f ? 0.f : __half2float(e[v]) * p.part_prev[r * p.ntiles + v / kStatW].x -
-                                          (v == y ? w : 0.f);
+      const float2 s = p.part_prev[r * p.ntiles + v / kStatW];
+      const float x = w == 0.f ? 0.f : (v == y ? s.y : __half2float(e[v]) * s.x);
       g[v] = __float2bfloat16_rn(x);
     }
   }
@@ -269,8 +272,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 32; ++j)
             if (g * 32 + j == (int)jy) zyv = __uint_as_float(r[g][j]);
       }
+      // s = sum of exp(z - m) over the tile less the term of one maximum (exactly 1): the
+      // other maxima count 1 each; kept apart so that the confident regime, where the
+      // rest is far below 1, does not round it away
       const float mb2 = m * L2E;
-      float s = 0.f;
+      float s = 0.f, nmax = -1.f;
       const uint32_t stg = saddr(stg_base + (warp - 2) * STG_BYTES);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -283,18 +289,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (ncol == 128) {
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float e0 = ex2(fmaf(__uint_as_float(r[g][j]), L2E, -mb2));
-            const float e1 = ex2(fmaf(__uint_as_float(r[g][j + 1]), L2E, -mb2));
-            s += e0 + e1;
+            const float z0 = __uint_as_float(r[g][j]), z1 = __uint_as_float(r[g][j + 1]);
+            const float e0 = ex2(fmaf(z0, L2E, -mb2));
+            const float e1 = ex2(fmaf(z1, L2E, -mb2));
+            s += (z0 == m ? 0.f : e0) + (z1 == m ? 0.f : e1);
+            nmax += (z0 == m ? 1.f : 0.f) + (z1 == m ? 1.f : 0.f);
             const __half2 hh = __floats2half2_rn(e0, e1);
             hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float e0 = (g * 32 + j < ncol) ? ex2(fmaf(__uint_as_float(r[g][j]), L2E, -mb2)) : 0.f;
-            const float e1 = (g * 32 + j + 1 < ncol) ? ex2(fmaf(__uint_as_float(r[g][j + 1]), L2E, -mb2)) : 0.f;
-            s += e0 + e1;
+            const float z0 = __uint_as_float(r[g][j]), z1 = __uint_as_float(r[g][j + 1]);
+            const bool in0 = g * 32 + j < ncol, in1 = g * 32 + j + 1 < ncol;
+            const float e0 = in0 ? ex2(fmaf(z0, L2E, -mb2)) : 0.f;
+            const float e1 = in1 ? ex2(fmaf(z1, L2E, -mb2)) : 0.f;
+            s += (in0 && z0 == m ? 0.f : e0) + (in1 && z1 == m ? 0.f : e1);
+            nmax += (in0 && z0 == m ? 1.f : 0.f) + (in1 && z1 == m ? 1.f : 0.f);
             const __half2 hh = __floats2half2_rn(e0, e1);
             hv[j / 2] = *reinterpret_cast<const uint32_t*>(&hh);
           }
@@ -318,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
       }
       const int64_t tix = (int64_t)nb * 2 + h;
-      if (vrow && tix < p.ntiles) p.part[(int64_t)row * p.ntiles + tix] = make_float2(m, s);
+      if (vrow && tix < p.ntiles) p.part[(int64_t)row * p.ntiles + tix] = make_float2(m, s + nmax);
       if (vrow && has_y) p.zy[row] = zyv;
       if (p.gprev) side_run(p, sj, quota);
     }

@@ -14,6 +14,14 @@ Recipe (numpy PCG64, one independent stream per quantity):
   GRPO advantages A ~ N(0, 1) per response, broadcast to its tokens; the noise
   added to the old log-probs ~ N(0, 0.1^2); DPO reference sequence log-probs
   ~ N(-2000, 50^2), float64.
+
+Peaked (confident-token) inputs, ``make_peaked``: W ~ N(0, (sigma_z / sqrt(d))^2) so that
+a row's logits spread with standard deviation about sigma_z, and every row of H is
+nudged towards its label's row of W, H_t += a_t W_{y_t} / (w_std^2 d) with a_t ~ U[lo, hi],
+which raises the label's logit by about a_t while moving the others by about
+a_t / sqrt(d).  With a_t well above the largest of V Gaussian logits most tokens are
+predicted with probability close to 1, the regime of a trained language-model head.
+The nudge is applied to the float32 draws, then both matrices are rounded.
 """
 from __future__ import annotations
 
@@ -22,7 +30,7 @@ import numpy as np
 IGNORE_INDEX = -100
 
 # one stream id per quantity so that changing one shape never shifts another draw
-_STREAM = {"H": 1, "W": 2, "labels": 3, "mask": 4, "adv": 5, "noise": 6, "ref": 7, "rows": 8}
+_STREAM = {"H": 1, "W": 2, "labels": 3, "mask": 4, "adv": 5, "noise": 6, "ref": 7, "rows": 8, "lift": 9}
 
 
 def rng_for(seed: int, what: str) -> np.random.Generator:
@@ -62,6 +70,25 @@ def make_hw(T: int, d: int, V: int, seed: int, dtype: str, w_std: float = 0.02):
     H = _normal(seed, "H", (T, d), 1.0, dtype == "bf16")
     W = _normal(seed, "W", (V, d), w_std, dtype == "bf16")
     return H, W
+
+
+def make_peaked(T: int, d: int, V: int, seed: int, dtype: str, sigma_z: float, lift_lo: float,
+                lift_hi: float, frac: float = 0.1):
+    """H [T, d], W [V, d] and labels [T] of the confident-token regime (see the module
+    docstring): the label's logit lifted by a_t ~ U[lift_lo, lift_hi] above a N(0,
+    sigma_z^2) background, ``frac`` of the tokens ignored by a permutation mask."""
+    if dtype not in ("bf16", "fp32"):
+        raise ValueError(dtype)
+    w_std = sigma_z / np.sqrt(d)
+    H = _normal(seed, "H", (T, d), 1.0, False)
+    W = _normal(seed, "W", (V, d), w_std, False)
+    y = make_labels(T, V, seed, "frac" if frac > 0 else "none", frac)
+    lab = rng_for(seed, "labels").integers(0, V, size=T, dtype=np.int64)   # the labels before masking
+    a = rng_for(seed, "lift").uniform(lift_lo, lift_hi, size=T).astype(np.float32)
+    H += (a / np.float32(w_std * w_std * d))[:, None] * W[lab]
+    if dtype == "bf16":
+        H, W = round_bf16(H), round_bf16(W)
+    return H, W, y
 
 
 def make_labels(T: int, V: int, seed: int, mask: str = "none", frac: float = 0.0,
