@@ -73,17 +73,26 @@ def make_hw(T: int, d: int, V: int, seed: int, dtype: str, w_std: float = 0.02):
 
 
 def make_peaked(T: int, d: int, V: int, seed: int, dtype: str, sigma_z: float, lift_lo: float,
-                lift_hi: float, frac: float = 0.1):
+                lift_hi: float, frac: float = 0.1, copies=(), labels=None):
     """H [T, d], W [V, d] and labels [T] of the confident-token regime (see the module
     docstring): the label's logit lifted by a_t ~ U[lift_lo, lift_hi] above a N(0,
-    sigma_z^2) background, ``frac`` of the tokens ignored by a permutation mask."""
+    sigma_z^2) background, ``frac`` of the tokens ignored by a permutation mask.
+
+    ``copies``: pairs (dst, src) of vocabulary rows; row dst of W becomes an exact copy of
+    row src before anything else, so the two logits are equal in every row.  ``labels``:
+    [T] labels to use (before the ignore mask) instead of the uniform draw."""
     if dtype not in ("bf16", "fp32"):
         raise ValueError(dtype)
     w_std = sigma_z / np.sqrt(d)
     H = _normal(seed, "H", (T, d), 1.0, False)
     W = _normal(seed, "W", (V, d), w_std, False)
+    for dst, src in copies:
+        W[dst] = W[src]
     y = make_labels(T, V, seed, "frac" if frac > 0 else "none", frac)
     lab = rng_for(seed, "labels").integers(0, V, size=T, dtype=np.int64)   # the labels before masking
+    if labels is not None:
+        lab = np.asarray(labels, dtype=np.int64)
+        y = np.where(y == IGNORE_INDEX, y, lab).astype(np.int32)
     a = rng_for(seed, "lift").uniform(lift_lo, lift_hi, size=T).astype(np.float32)
     H += (a / np.float32(w_std * w_std * d))[:, None] * W[lab]
     if dtype == "bf16":

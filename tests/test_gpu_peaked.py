@@ -83,3 +83,81 @@ def test_sft_peaked_parity(sbp, name, chunk):
     # the confident tokens' own rows: their gradient is the small difference p - onehot
     conf = np.nonzero(valid)[0][py > 0.999]
     assert rel_fro(dH[conf], ref["dH"][conf]) <= tol["grad"]
+
+
+def tied_case(dtype, T=300, d=256, V=2000):
+    """Peaked inputs in which some vocabulary rows of W are exact copies of others, within
+    one 128-column tile (6 = 5, 901 = 900) and across tiles (1290 = 5), and every fourth
+    token's label sits on a copied row: those tokens' logit maxima are tied exactly."""
+    lab = I.rng_for(77, "labels").integers(0, V, size=T)
+    pick = np.arange(0, T, 4)
+    lab[pick] = np.where(np.arange(len(pick)) % 2 == 0, 5, 900)
+    return I.make_peaked(T, d, V, 77, dtype, 10.0, 40.0, 70.0, frac=0.1,
+                         copies=((6, 5), (1290, 5), (901, 900)), labels=lab)
+
+
+@pytest.mark.parametrize("dtype,chunk", [("bf16", 128), ("fp32", 64)])
+def test_sft_tied_maxima(sbp, dtype, chunk):
+    """Exactly equal logits at a row's maximum (in one tile and in different tiles): the
+    tile sums count each further copy of the maximum as 1, and the label's entry w (p_y - 1)
+    comes out as it should (for a two-way tie with nothing else left, -w/2)."""
+    H, W, y = tied_case(dtype)
+    ref = O.sft(H, W, y, IGN)
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    out = sbp.sft(Ht, Wt, yt, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    tol = TOL[dtype]
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= tol["loss"], (out["loss"].item(), ref["loss"])
+    dH = out["dH"].float().cpu().numpy()
+    assert rel_fro(dH, ref["dH"]) <= tol["grad"]
+    assert rel_fro(out["dW"].cpu().numpy(), ref["dW"]) <= tol["grad"]
+    tied = np.nonzero(np.isin(y, [5, 900]))[0]
+    assert rel_fro(dH[tied], ref["dH"][tied]) <= tol["grad"]
+    # most tied tokens put almost all their probability on the copies of their label,
+    # split evenly: p_y close to 1/2 (label 900, two copies) or 1/3 (label 5, three)
+    py = np.exp(ref["logp"][tied])
+    assert np.mean(np.abs(py - np.where(y[tied] == 5, 1 / 3, 1 / 2)) < 0.01) > 0.6
+
+
+def test_grpo_peaked_parity(sbp):
+    """GRPO in the confident regime (per-token weights A r / N instead of 1 / N)."""
+    H, W, y, ref_sft = case("bf16_T1000_d1024_V151936")
+    T = H.shape[0]
+    f_logp = ref_sft["logp"]
+    A = I.make_advantages(4, (T + 3) // 4, 31)[:T].astype(np.float32)
+    lpo = (f_logp + I.make_logp_noise(T, 31)).astype(np.float32)
+    Ht, Wt, yt = to_dev(torch, H, W, y, "bf16")
+    out = sbp.grpo(Ht, Wt, yt, torch.from_numpy(A).cuda(), torch.from_numpy(lpo).cuda(), 384)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.grpo(H, W, y, A.astype(np.float64), lpo.astype(np.float64), IGN)
+    tol = TOL["bf16"]
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= tol["loss"]
+    assert rel_fro(out["dH"].float().cpu().numpy(), ref["dH"]) <= tol["grad"]
+    assert rel_fro(out["dW"].cpu().numpy(), ref["dW"]) <= tol["grad"]
+
+
+def test_dpo_peaked_parity(sbp):
+    """DPO in the confident regime: sequence sums of mostly tiny log-probs, both passes."""
+    H, W, y, _ = case("bf16_T1000_d1024_V151936")
+    lens = [300, 200, 260, 240]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    p1 = O.dpo_pass1(H, W, y, cu, IGN)
+    Sref = p1["seq_logp"] + np.array([-2.0, 1.0, 3.0, -1.0])
+    Ht, Wt, yt = to_dev(torch, H, W, y, "bf16")
+    cut = torch.from_numpy(cu).cuda()
+    g1 = sbp.dpo_pass1(Ht, Wt, yt, cut, 256)
+    g2 = sbp.dpo_pass2(Ht, Wt, yt, cut, g1["seq_logp"], torch.from_numpy(Sref).cuda(), 0.5, 256)
+    torch.cuda.synchronize()
+    sbp.check_status(g1["status"])
+    sbp.check_status(g2["status"])
+    ref = O.dpo(H, W, y, cu, Sref, 0.5, IGN)
+    tol = TOL["bf16"]
+    S = g1["seq_logp"].cpu().numpy()
+    assert np.max(np.abs(S - ref["seq_logp"]) / np.abs(ref["seq_logp"])) <= tol["seq"]
+    assert rel(g2["loss"].item(), ref["loss"]) <= tol["loss"]
+    assert rel_fro(g2["dH"].float().cpu().numpy(), ref["dH"]) <= tol["grad"]
+    assert rel_fro(g2["dW"].cpu().numpy(), ref["dW"]) <= tol["grad"]
