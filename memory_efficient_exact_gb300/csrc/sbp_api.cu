@@ -609,10 +609,8 @@ int validate(const Call& c, Layout* L) {
   if (c.dtype == SBP_BF16 && (c.d % 8 != 0 || c.V % 8 != 0)) return SBP_ERR_UNSUPPORTED;
   if ((c.H && !al16(c.H)) || !al16(c.W) || (c.dH && !al16(c.dH)) || (c.dW && !al16(c.dW)))
     return SBP_ERR_ALIGNMENT;
-  if (c.dtype == SBP_FP32 && c.d % 4 != 0 && c.dH) {
-    // fp32 dH rows are written 4 at a time only when d % 4 == 0; other d take the
-    // scalar tail path, which needs no alignment beyond the element size.
-  }
+  // (fp32 dH rows are written 4 at a time only when d % 4 == 0; other d take the scalar
+  // tail path, which needs no alignment beyond the element size.)
   if (!c.ws || (reinterpret_cast<uintptr_t>(c.ws) & 255u) || c.ws_bytes < L->total) return SBP_ERR_WORKSPACE;
   return SBP_OK;
 }

@@ -229,6 +229,9 @@ def test_edge_cases(sbp, dtype):
     ("bf16", 100, 128, 1000, 64, "last"),     # every label on the last column (V-tail tile)
     ("fp32", 100, 32, 333, 64, "last"),
     ("bf16", 300, 128, 1000, 128, "zero"),    # every label on column 0
+    ("fp32", 40, 64, 1, 8, None),             # V = 1: loss 0 and zero gradients exactly
+    ("fp32", 50, 64, 7, 16, None),            # V inside one 8-column vector of the gradient pass
+    ("bf16", 50, 64, 8, 16, None),            # the smallest bf16 vocabulary (rows of 16 bytes)
 ])
 def test_edge_shapes_and_labels(sbp, dtype, T, d, V, chunk, label):
     H, W, y = make_case(T, d, V, dtype, seed=23 + T + d, w_std=0.2)
@@ -243,6 +246,10 @@ def test_edge_shapes_and_labels(sbp, dtype, T, d, V, chunk, label):
     ref = O.sft(H, W, y, IGN)
     tol = TOL[dtype]
     assert int(out["n_valid"].item()) == ref["n_valid"]
+    if V == 1:
+        assert out["loss"].item() == 0.0 and torch.count_nonzero(out["dH"]).item() == 0
+        assert torch.count_nonzero(out["dW"]).item() == 0
+        return
     assert rel(out["loss"].item(), ref["loss"]) <= tol["loss"]
     check_grads(dtype, out, ref, y)
 
