@@ -117,6 +117,9 @@ struct BwdP {
   // z * zr_h and writes dW rows from z * zr_dw (all 0 when batch = 1)
   int batch, n_dh_b, n_dw_b;
   int zr_g, zr_w, zr_h, zr_dw;
+  // 1: the MN-major map of G / W / H is the three-dimensional one that loads 128 columns
+  // in one copy (make_map_mn2); 0: the two-dimensional 64 x 64 one, two copies
+  int mn2_g, mn2_w, mn2_h;
 };
 
 // k_bwd stages its dW output through shared memory: one 32x32 fp32 block (4 KB, 128-byte
@@ -426,17 +429,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (rank == 0) mbar_expect_tx(&c->full[stage], PAIR_TX);
           if (w.kind == 0) {
             tma_load_2d_pair(sa, &tmGk, fb, kb * BK, w.z * p.zr_g + mrow);
+            const int wr = w.z * p.zr_w + kb * BK;
+            if (p.mn2_w) {
+              tma_load_3d_pair(sb, &tmWmn, fb, 0, wr, ncol / 64);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(sb + j * BOX_BYTES, &tmWmn, fb, ncol + j * 64, w.z * p.zr_w + kb * BK);
+              for (int j = 0; j < 2; ++j) tma_load_2d_pair(sb + j * BOX_BYTES, &tmWmn, fb, ncol + j * 64, wr);
+            }
           } else {
+            const int gr = w.z * p.zr_g + kb * BK;
+            if (p.mn2_g) {
+              tma_load_3d_pair(sa, &tmGmn, fb, 0, gr, mrow / 64);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(sa + j * BOX_BYTES, &tmGmn, fb, mrow + j * 64, w.z * p.zr_g + kb * BK);
+              for (int j = 0; j < 2; ++j) tma_load_2d_pair(sa + j * BOX_BYTES, &tmGmn, fb, mrow + j * 64, gr);
+            }
+            const int hr = (int)(w.z * (int64_t)p.zr_h + p.r0 + (int64_t)kb * BK);
+            if (p.mn2_h) {
+              tma_load_3d_pair(sb, &tmHmn, fb, 0, hr, ncol / 64);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(sb + j * BOX_BYTES, &tmHmn, fb, ncol + j * 64,
-                               (int)(w.z * (int64_t)p.zr_h + p.r0 + (int64_t)kb * BK));
+              for (int j = 0; j < 2; ++j) tma_load_2d_pair(sb + j * BOX_BYTES, &tmHmn, fb, ncol + j * 64, hr);
+            }
           }
           issued |= 1u << stage;
           last_phase[stage] = phase;
@@ -642,9 +656,14 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   const uint64_t h_rows = a.h_rows ? (uint64_t)a.h_rows : (uint64_t)a.T;
   const uint64_t dw_rows = a.dw_rows ? (uint64_t)a.dw_rows : (uint64_t)a.V;
   if (!make_map(&mGk, a.G, (uint64_t)a.V, g_rows, (uint64_t)a.ldg, BK, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mGmn, a.G, (uint64_t)a.V, g_rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&mWmn, a.W, (uint64_t)a.d, w_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&mHmn, a.H, (uint64_t)a.d, h_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  // MN-major operands: one copy of 128 columns where the row length allows it (multiples of
+  // 64 elements), else two 64 x 64 boxes
+  const int mn2_g = make_map_mn2(&mGmn, a.G, g_rows, (uint64_t)a.ldg) ? 1 : 0;
+  if (!mn2_g && !make_map(&mGmn, a.G, (uint64_t)a.V, g_rows, (uint64_t)a.ldg, 64, 64)) return cudaErrorInvalidValue;
+  const int mn2_w = make_map_mn2(&mWmn, a.W, w_rows, (uint64_t)a.d) ? 1 : 0;
+  if (!mn2_w && !make_map(&mWmn, a.W, (uint64_t)a.d, w_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
+  const int mn2_h = make_map_mn2(&mHmn, a.H, h_rows, (uint64_t)a.d) ? 1 : 0;
+  if (!mn2_h && !make_map(&mHmn, a.H, (uint64_t)a.d, h_rows, (uint64_t)a.d, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap mDW, mDH;
   if (!make_map_f32(&mDW, a.dW, (uint64_t)a.d, dw_rows)) return cudaErrorInvalidValue;
   // dH partials [splits * batch planes][rows][d] fp32: a 3-D map, so that stores clip at
@@ -670,6 +689,7 @@ cudaError_t tc_backward(const TcBwdArgs& a, cudaStream_t s) {
   p.n_dh = p.n_dh_b * p.batch;
   p.n_total = p.n_dh + p.n_dw_b * p.batch;
   p.zr_g = a.zr_g; p.zr_w = a.zr_w; p.zr_h = a.zr_h; p.zr_dw = a.zr_dw;
+  p.mn2_g = mn2_g; p.mn2_w = mn2_w; p.mn2_h = mn2_h;
   p.dh_part = a.dh_part; p.plane = (int64_t)a.rows * a.d;
   p.dW = a.dW; p.dw_acc = a.dw_accumulate;
   p.counter = a.counter; p.status = a.status; p.limit_ns = wait_limit_ns();

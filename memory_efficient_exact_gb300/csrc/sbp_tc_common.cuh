@@ -211,6 +211,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar_cluster)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar_cluster, int x,
+                                                 int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar_cluster)
+      : "memory");
+}
 __device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
@@ -436,6 +444,26 @@ inline bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
   cuuint32_t box[2] = {box_in, box_out};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MN-major bf16 operand map that loads 128 columns in one copy: the [outer, row_elems]
+// matrix (row_elems a multiple of 64) seen as [row_elems / 64][outer][64], box 64 x 64 x 2.
+// The two 64-column blocks land 8 KB apart in shared memory with the 128-byte swizzle,
+// exactly where two 64 x 64 boxes of the two-dimensional map would.  Columns of the last
+// block are real memory of the row (row_elems is the row stride), so nothing past the
+// allocation is read; columns past the matrix's logical width hold what the buffer holds
+// there, which only reaches outputs that the stores clip.
+inline bool make_map_mn2(CUtensorMap* m, const void* ptr, uint64_t outer, uint64_t row_elems) {
+  if (row_elems % 64 != 0) return false;
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, outer, row_elems / 64};
+  cuuint64_t strides[2] = {row_elems * 2, 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
