@@ -100,7 +100,7 @@ struct TcFwdArgs {
   float2* part; float* zy;
   int32_t* status;
   // optional: the previous chunk's logit gradient, formed in place by this launch's
-  // epilogue warps between tiles (G = e * scale - w [v = y], fp16 -> bf16)
+  // epilogue warps between tiles (G = e * scale, w expm1(logp) at the label; fp16 -> bf16)
   void* gprev = nullptr; const float2* part_prev = nullptr; const float* w_prev = nullptr;
   const int32_t* y_prev = nullptr; int rows_prev = 0;
 };
