@@ -33,7 +33,9 @@
  *   multiples of 8 (16-byte rows for the tensor-memory-access unit).
  * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *   only enqueues work on it and returns; nothing synchronises the host.  Calls on
- *   different streams need distinct workspaces.
+ *   different streams need distinct workspaces.  A call can be captured into a CUDA
+ *   graph from `stream` and replayed (the same results bit for bit); make one plain call
+ *   on the device first, which sets up the library's per-device state.
  * Errors: the return value is an sbp_status.  Argument errors are found on the host
  *   and returned before anything is enqueued (outputs untouched).  Errors only the
  *   device can see (a label outside [0, V) other than ignore_index; a pipeline wait

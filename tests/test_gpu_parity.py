@@ -383,3 +383,60 @@ def test_fp32_golden_fixtures(sbp, chunk):
     assert np.max(np.abs(p1["seq_logp"].cpu().numpy() - S) / np.abs(S)) <= tol["seq"]
     assert rel(p2["loss"].item(), want["loss"]) <= tol["loss"]
     grads(p2, want)
+
+
+def test_lmhead_calls_under_graph_capture(sbp):
+    """The LM-head calls only enqueue work on the caller's stream (the host-buffer call also
+    forks the library's side stream from it and joins it back): each can be captured into
+    a CUDA graph and replayed, and a replay gives the bits of a plain call.  SFT, GRPO, both
+    DPO passes in one graph, and the host-buffer SFT call with page-locked host arrays."""
+    T, d, V, chunk = 700, 256, 2000, 256
+    H, W, y = make_case(T, d, V, "bf16", seed=91, w_std=0.1)
+    Ht, Wt, yt = to_dev(torch, H, W, y, "bf16")
+    f = O.forward(H, W, y, IGN)
+    A = torch.from_numpy(I.make_advantages(4, (T + 3) // 4, 91)[:T].astype(np.float32)).cuda()
+    lpo = torch.from_numpy((f["logp"] + I.make_logp_noise(T, 91)).astype(np.float32)).cuda()
+    cu = torch.tensor([0, 200, 350, 550, 700], dtype=torch.int32, device="cuda")
+    sref = torch.tensor([-7000.0, -5000.0, -7100.0, -4900.0], dtype=torch.float64, device="cuda")
+    s = torch.cuda.Stream()
+    mk = lambda mode: sbp.make_workspace(T, d, V, chunk, sbp.BF16, mode)
+    ws = {m: mk(m) for m in (sbp.MODE_SFT, sbp.MODE_GRPO, sbp.MODE_DPO1, sbp.MODE_DPO2)}
+    st = torch.zeros((), dtype=torch.int32, device="cuda")
+    dH, dW = torch.empty_like(Ht), torch.empty((V, d), dtype=torch.float32, device="cuda")
+    Hh = torch.from_numpy(H).to(torch.bfloat16).pin_memory()
+    yh = torch.from_numpy(y).pin_memory()
+    dHh = torch.empty(Hh.shape, dtype=torch.bfloat16).pin_memory()
+    lossh = torch.empty((), dtype=torch.float32).pin_memory()
+    nvh = torch.empty((), dtype=torch.int64).pin_memory()
+    hws = torch.empty(sbp.host_workspace_bytes(T, d, V, chunk, sbp.BF16), dtype=torch.uint8, device="cuda")
+    calls = {
+        "sft": lambda: sbp.sft(Ht, Wt, yt, chunk, dH=dH, dW=dW, workspace=ws[sbp.MODE_SFT], status=st, stream=s),
+        "grpo": lambda: sbp.grpo(Ht, Wt, yt, A, lpo, chunk, dH=dH, dW=dW, workspace=ws[sbp.MODE_GRPO], status=st,
+                                 stream=s),
+        "dpo": lambda: sbp.dpo_pass2(Ht, Wt, yt, cu, sbp.dpo_pass1(Ht, Wt, yt, cu, chunk, workspace=ws[sbp.MODE_DPO1],
+                                                                  status=st, stream=s)["seq_logp"],
+                                     sref, 0.5, chunk, dH=dH, dW=dW, workspace=ws[sbp.MODE_DPO2], status=st,
+                                     stream=s),
+        "host": lambda: sbp.sft_host(Hh, Wt, yh, chunk, dH=dHh, dW=dW, loss=lossh, n_valid=nvh, workspace=hws,
+                                     status=st, stream=s),
+    }
+    for name, call in calls.items():
+        # a plain call (which also sets up the library's per-device state), then a capture
+        with torch.cuda.stream(s):
+            out = call()
+        s.synchronize()
+        sbp.check_status(st, name)
+        ref = {"dH": (dHh if name == "host" else dH).clone(), "dW": dW.clone(),
+               "loss": (lossh if name == "host" else out["loss"]).clone()}
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            out = call()
+        for _ in range(2):
+            dW.zero_()
+            (dHh if name == "host" else dH).zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            sbp.check_status(st, name)
+            assert torch.equal((dHh if name == "host" else dH), ref["dH"]), name
+            assert torch.equal(dW, ref["dW"]), name
+            assert torch.equal((lossh if name == "host" else out["loss"]), ref["loss"]), name
