@@ -15,7 +15,10 @@ N > 1 runs under torchrun, one rank per GPU; every rank processes its own batch
 ``--impl reference`` times the float64 CPU oracle on a bounded sample of the same
 workload instead (rank 0 only).
 
-Other lines (each its own JSON line; not the driver's):
+The plain invocation also measures the other workloads -- GRPO, DPO, the two chunk
+sweeps and the two sublayers, each in its own process after the main line's measurement --
+and folds their JSON lines under "other_workloads" (`--no-other-workloads` skips that).
+Other lines (each its own JSON line when run by itself):
   --objective grpo|dpo          the other objectives (8 x 2048 / 8 x 4096 tokens)
   --workload sft_T8192_d2560|sft_T65536_d5120 [--chunk C]   the chunk-sweep workloads
   --workload profile            a small case of the same kernels for ncu captures
@@ -211,6 +214,42 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------------------- ours
+
+# The other workloads of the input recipes and the two sublayers, each measured by its own
+# bench process after the main line (the plain invocation only); their JSON lines are
+# folded into the main line under "other_workloads", so that one run records them all.
+OTHER_WORKLOADS = [
+    ("grpo_8x2048_d4096_chunk4096", ["--objective", "grpo", "--steps", "10"]),
+    ("dpo_8x4096_d4096_chunk4096", ["--objective", "dpo", "--steps", "5"]),
+    ("sft_T8192_d2560_chunk512", ["--workload", "sft_T8192_d2560", "--chunk", "512", "--steps", "10"]),
+    ("sft_T8192_d2560_chunk1024", ["--workload", "sft_T8192_d2560", "--chunk", "1024", "--steps", "10"]),
+    ("sft_T8192_d2560_chunk2048", ["--workload", "sft_T8192_d2560", "--chunk", "2048", "--steps", "10"]),
+    ("sft_T65536_d5120_chunk4096", ["--workload", "sft_T65536_d5120", "--chunk", "4096", "--steps", "3"]),
+    ("attn_H32_T8192_hd128_chunk1024", ["--sublayer", "attn", "--steps", "5"]),
+    ("attn_H32_Hkv8_T8192_hd128_chunk1024", ["--sublayer", "attn", "--steps", "5", "--kv-heads", "8"]),
+    ("mlp_T16384_d4096_f12288_chunk4096", ["--sublayer", "mlp", "--steps", "5"]),
+]
+OTHER_KEYS = ("metric", "value", "unit", "ms_per_step", "steps", "dtype", "config", "roofline", "pct_bf16_peak",
+              "pct_bf16_peak_executed", "peak_mem_gb", "e2e", "clocks", "gpu_launches")
+
+
+def run_other_workloads(timeout_s: float = 240.0) -> dict:
+    out = {}
+    for name, extra in OTHER_WORKLOADS:
+        cmd = [sys.executable, os.path.abspath(__file__), *extra, "--no-cpu-baseline", "--no-other-workloads"]
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=timeout_s, cwd=ROOT)
+            lines = [x for x in r.stdout.strip().splitlines() if x.startswith("{")]
+            if r.returncode != 0 or not lines:
+                out[name] = {"error": f"rc={r.returncode}: " + (r.stderr.strip().splitlines() or [""])[-1][:200]}
+                continue
+            d = json.loads(lines[-1])
+            out[name] = {k: d[k] for k in OTHER_KEYS if k in d}
+            out[name]["command"] = "python bench.py " + " ".join(extra)
+        except (subprocess.TimeoutExpired, OSError, ValueError) as e:
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    return out
+
 
 def run_ours(args):
     import numpy as np
@@ -441,6 +480,10 @@ def run_ours(args):
         "loss": loss,
         "cpu_baseline": cpu,
     }
+    if getattr(args, "other_workloads", False) and world == 1:
+        # the other lines run in their own processes (this one keeps under 7 GB meanwhile)
+        torch.cuda.empty_cache()
+        line["other_workloads"] = run_other_workloads()
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -780,6 +823,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="plain invocation: skip the other workloads' lines folded into the main line")
     ap.add_argument("--comparator", choices=["torch"], default=None,
                     help="time the same chunked LM head in eager PyTorch instead (a comparison line only)")
     ap.add_argument("--workload", choices=["main", "profile"] + sorted(SWEEP_WORKLOADS), default="main",
@@ -822,6 +867,10 @@ def main(argv=None):
                                 f"_chunk{WORKLOAD['chunk']}")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    # the other workloads' lines ride along with the main line of a plain invocation only
+    args.other_workloads = (not args.no_other_workloads and args.workload == "main" and args.objective == "sft"
+                            and args.sublayer == "lmhead" and args.comparator is None and args.chunk is None
+                            and args.tokens is None and args.d is None and not args.lean)
     if args.impl == "reference":
         return run_reference(args)
     if args.comparator == "torch":

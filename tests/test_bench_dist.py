@@ -67,12 +67,25 @@ def _args_of(argv):
     seen = {}
 
     def rec(args):
-        seen.update(dict(b.WORKLOAD), chunk_arg=args.chunk, sublayer=args.sublayer)
+        seen.update(dict(b.WORKLOAD), chunk_arg=args.chunk, sublayer=args.sublayer,
+                    other=getattr(args, "other_workloads", None), others=list(b.OTHER_WORKLOADS))
         return 0
     b.run_ours = b.run_mlp_bench = b.run_attn_bench = rec
     b.run_reference = rec
     assert b.main(argv) == 0
     return seen
+
+
+def test_other_workloads_ride_only_with_the_plain_invocation():
+    # the plain invocation folds the other workloads' lines into its own; any flag that
+    # picks another workload, schedule or sublayer measures that one alone
+    assert _args_of([])["other"] is True and _args_of(["--steps", "2"])["other"] is True
+    for argv in (["--no-other-workloads"], ["--chunk", "2048"], ["--objective", "grpo"], ["--workload", "profile"],
+                 ["--lean"], ["--sublayer", "mlp"], ["--tokens", "8192"]):
+        assert _args_of(argv)["other"] is False, argv
+    others = _args_of([])["others"]
+    names = [n for n, _ in others]
+    assert len(set(names)) == len(names) and len(names) == 9
 
 
 def test_bench_workload_selection():
