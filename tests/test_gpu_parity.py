@@ -54,6 +54,8 @@ SFT_CASES = [
     ("bf16", 130, 72, 264, 64, 0.2),        # K tail (72 = 64 + 8)
     ("bf16", 1000, 512, 4096, 384, 0.04),   # many tiles in every dimension
     ("bf16", 640, 1024, 8200, 640, 0.03),   # d spans 4 N tiles, V spans 33 (tail of 8)
+    ("bf16", 96, 128, 262144, 64, 0.05),    # a vocabulary of 2^18 (2048 statistics tiles per row)
+    ("bf16", 300, 8192, 4096, 256, 0.01),   # d = 8192 (32 N tiles, 128 k-blocks per forward tile)
 ]
 
 
