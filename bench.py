@@ -187,6 +187,18 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def blas_info() -> str:
+    """The BLAS numpy (and so the oracle) uses, and its thread limit where set."""
+    import numpy as np
+    try:
+        b = np.show_config(mode="dicts")["Build Dependencies"]["blas"]
+        name = f"{b.get('name', '?')} {b.get('version', '')}".strip()
+    except Exception:
+        name = "unknown"
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or "default (all cores)"
+    return f"{name}, threads {threads}"
+
+
 # --------------------------------------------------------------------------------- reference
 
 def run_reference(args):
@@ -206,7 +218,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sec / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {k: w[k] for k in ("workload", "T", "d", "V", "chunk")},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample,
+                         "blas": blas_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -434,7 +447,8 @@ def run_ours(args):
         Ts = CPU_SAMPLE_TOKENS
         sec = cpu_oracle_sample(H, W, y, Ts)
         cpu = {"value": Ts / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"first {Ts} of the {T} tokens (full V={V}, d={d}), float64 numpy/BLAS, one run"}
+               "sample": f"first {Ts} of the {T} tokens (full V={V}, d={d}), float64 numpy/BLAS, one run",
+               "blas": blas_info()}
 
     metric = METRIC if (objective, d, V) == ("sft", 4096, 151936) else \
         f"lm_head fwd+bwd tokens/s ({objective}, d={d}, V={V})"
