@@ -775,7 +775,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
     __syncwarp();
   } else {
     const int q = warp & 3, cg = (warp - 2) >> 2;   // lane quadrant, 32-column group
-    const int lrow = q * 32 + lane;
     const uint32_t trow = (uint32_t)(q * 32) << 16;
     const float sl2 = p.scale * L2E;
     uint32_t tfull_seen = 0, g = 0;

@@ -117,7 +117,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
-    const int lrow = q * 32 + lane;
     uint64_t* bar = lbar + (warp - 2);
     uint32_t lphase = 0;
     if (DA) {
@@ -132,8 +131,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int mp = tile % p.mt, nb = tile / p.mt;
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      const int row = mp * 256 + (int)rank * 128 + lrow;
-      const bool vrow = row < p.rows;
       if (!warp_wait_cluster(&c->tfull[buf], use & 1u, c, p.limit_ns)) {
         fail(c, p.status);
         break;

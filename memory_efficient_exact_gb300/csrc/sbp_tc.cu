@@ -509,7 +509,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
-    const int lrow = q * 32 + lane;
     int local = 0;
     for (int i = 0;; ++i, ++local) {
       const int slot = i % RING;
