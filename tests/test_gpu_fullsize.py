@@ -84,6 +84,27 @@ def test_sft_T8192_d2560(sbp, c2, chunk):
     check_sampled(H, W, y, w, c2["lse"], out, rows, vocab_sample(y, W.shape[0], chunk), f" chunk={chunk}")
 
 
+def test_sft_T8192_d2560_prefix_full_dW(sbp, c2):
+    """The first 4096 tokens as a problem of their own at chunk 1024: the first chunk is the
+    1024-token prompt, every label ignored, so one whole chunk contributes nothing while
+    the later ones accumulate into dW; full dH and full dW against the unchunked oracle."""
+    Tp = 4096
+    H, W = np.ascontiguousarray(c2["H"][:Tp]), c2["W"]
+    y = np.ascontiguousarray(c2["labels"][:Tp])
+    assert np.all(y[:1024] == IGN)
+    Ht, Wt, yt = dev_inputs(H, W, y)
+    out = sbp.sft(Ht, Wt, yt, 1024)
+    torch.cuda.synchronize()
+    sbp.check_status(out["status"])
+    ref = O.sft(H, W, y, IGN)
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert rel(out["loss"].item(), ref["loss"]) <= BF["loss"]
+    dH = out["dH"].float().cpu().numpy()
+    assert rel_fro(dH, ref["dH"]) <= BF["grad"]
+    assert rel_fro(out["dW"].cpu().numpy(), ref["dW"]) <= BF["grad"]
+    assert np.all(dH[:1024] == 0.0)
+
+
 @pytest.fixture(scope="module")
 def c3():
     return I.make_workload("grpo_bf16_8x2048_d4096_V151936")
