@@ -442,3 +442,39 @@ def test_lmhead_calls_under_graph_capture(sbp):
             assert torch.equal((dHh if name == "host" else dH), ref["dH"]), name
             assert torch.equal(dW, ref["dW"]), name
             assert torch.equal((lossh if name == "host" else out["loss"]), ref["loss"]), name
+
+
+def test_host_buffer_calls_from_two_threads(sbp):
+    """Host-buffer calls from two host threads on two streams share the library's
+    per-device side stream (taken under its lock for each call's enqueue): each gives the
+    bits of a call made alone."""
+    import threading
+    T, d, V, chunk = 900, 256, 2000, 256
+    cases = []
+    for seed in (5, 6):
+        H, W, y = make_case(T, d, V, "bf16", seed=seed, w_std=0.1)
+        Wt = torch.from_numpy(W).cuda().to(torch.bfloat16)
+        Hh = torch.from_numpy(H).to(torch.bfloat16).pin_memory()
+        yh = torch.from_numpy(y).pin_memory()
+        ref = sbp.sft_host(Hh, Wt, yh, chunk)
+        torch.cuda.synchronize()
+        sbp.check_status(ref["status"])
+        cases.append((Hh, Wt, yh, {k: v.clone() for k, v in ref.items() if k in ("dH", "dW", "loss")}))
+    outs = [None, None]
+
+    def run(i):
+        Hh, Wt, yh, _ = cases[i]
+        si = torch.cuda.Stream()
+        for _ in range(3):   # repeated, so the two threads' calls interleave
+            outs[i] = sbp.sft_host(Hh, Wt, yh, chunk, stream=si)
+        si.synchronize()
+    th = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    torch.cuda.synchronize()
+    for i in range(2):
+        sbp.check_status(outs[i]["status"])
+        for k in ("dH", "dW", "loss"):
+            assert torch.equal(outs[i][k], cases[i][3][k]), (i, k)
