@@ -144,7 +144,7 @@ __device__ __forceinline__ void fail_f(CtrlF* c, int32_t* status) {
 // thread already waited for.  Bounded like every other wait.
 __device__ __forceinline__ bool wait_n(uint64_t* b, uint32_t& seen, uint32_t need, CtrlF* c, uint64_t limit) {
   while (seen < need) {
-    if (!wait_cluster(b, seen & 1u, &c->abort, limit)) return false;
+    if (!wait_inl<true>(b, seen & 1u, &c->abort, limit)) return false;
     ++seen;
   }
   return true;
@@ -152,7 +152,7 @@ __device__ __forceinline__ bool wait_n(uint64_t* b, uint32_t& seen, uint32_t nee
 // The same for a whole warp (seen and need are warp-uniform).
 __device__ __forceinline__ bool warp_wait_n(uint64_t* b, uint32_t& seen, uint32_t need, CtrlF* c, uint64_t limit) {
   while (seen < need) {
-    if (!__all_sync(0xffffffffu, wait_cluster(b, seen & 1u, &c->abort, limit))) return false;
+    if (!__all_sync(0xffffffffu, wait_inl<true>(b, seen & 1u, &c->abort, limit))) return false;
     ++seen;
   }
   return true;
@@ -290,7 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       for (int u = pid; u < p.n_units && ok; u += npairs) {
         int zk, kp, b0, nblk;
         kv_unit(p, u, zk, kp, b0, nblk);
-        if (!wait_bounded(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        if (!wait_inl<false>(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
         const uint32_t fr = mapa(saddr(&c->rfull), 0);
         if (rank == 0) mbar_expect_tx(&c->rfull, 4u * 32768u);
         const int krow = 256 * kp + 128 * (int)rank;
@@ -305,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         for (int n = 0; n < nblk; ++n) {
           int z, b;
           kv_block(p, zk, b0, n, z, b);
-          if (!wait_bounded(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          if (!wait_inl<false>(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fa = mapa(saddr(&c->afull[sa]), 0);
           if (rank == 0) mbar_expect_tx(&c->afull[sa], 2u * KV_A_STAGE);
           const uint32_t st = sb + KV_A + sa * KV_A_STAGE;
@@ -323,9 +323,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       if (!ok) {
         fail_f(c, p.status);
         if (rank == 0) {
-          if (iss & 4u) wait_bounded(&c->rfull, lph_r, nullptr, 200000000ull);
+          if (iss & 4u) wait_inl<false>(&c->rfull, lph_r, nullptr, 200000000ull);
           for (int s = 0; s < 2; ++s)
-            if (iss & (1u << s)) wait_bounded(&c->afull[s], lph_a[s], nullptr, 200000000ull);
+            if (iss & (1u << s)) wait_inl<false>(&c->afull[s], lph_a[s], nullptr, 200000000ull);
         }
       }
     } else if (lane == 16) {
@@ -340,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         for (int n = 0; n < nblk; ++n) {
           int z, b;
           kv_block(p, zk, b0, n, z, b);
-          if (!wait_bounded(&c->bempty[0], phb ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          if (!wait_inl<false>(&c->bempty[0], phb ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fb = mapa(saddr(&c->bfull[0]), 0);
           if (rank == 0) mbar_expect_tx(&c->bfull[0], 4u * 16384u);
           const int qrow = p.c0 + 128 * b;
@@ -353,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       }
       if (!ok) {
         fail_f(c, p.status);
-        if (rank == 0 && any) wait_bounded(&c->bfull[0], lph, nullptr, 200000000ull);
+        if (rank == 0 && any) wait_inl<false>(&c->bfull[0], lph, nullptr, 200000000ull);
       }
     }
   } else if (warp == 1) {
@@ -367,7 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       // dV += P^T dO and dK += dS^T Q for global block gg (the first of its unit overwrites)
       auto accumulate = [&](uint32_t gg, bool first) -> bool {
         if (!wait_n(&c->oready, oready_seen, gg + 1, c, p.limit_ns)) return false;
-        if (!wait_bounded(&c->bfull[0], phb, &c->abort, p.limit_ns)) return false;
+        if (!wait_inl<false>(&c->bfull[0], phb, &c->abort, p.limit_ns)) return false;
         phb ^= 1u;
         if (first && !wait_n(&c->accempty, acc_seen, (uint32_t)lu, c, p.limit_ns)) return false;
         tc_fence_after();
@@ -386,14 +386,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
         int zk, kp, b0, nbl;
         kv_unit(p, u, zk, kp, b0, nbl);
-        if (!wait_bounded(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
+        if (!wait_inl<false>(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
         phr ^= 1u;
         tc_fence_after();
         for (int n = 0; n < nbl; ++n, ++g) {
           // S^T and dP^T of block g; the previous block's accumulation follows, so the
           // epilogue's work on block g overlaps it
           if (!wait_n(&c->tempty, tempty_seen, g, c, p.limit_ns)) { ok = false; break; }
-          if (!wait_bounded(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
+          if (!wait_inl<false>(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dst = dplus(dA, sa * KV_A_STAGE);
 #pragma unroll
@@ -415,7 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       }
       if (!ok) fail_f(c, p.status);
       commit2_mc(&c->mdone, 1);
-      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
+      wait_inl<false>(&c->mdone, 0, nullptr, 200000000ull);
     }
     __syncwarp();
   } else if (warp == KV_FWD_WARP) {
@@ -642,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
       for (int u = pid; u < p.n_units && ok; u += npairs) {
         int z, qp, nj;
         q_unit(p, u, z, qp, nj);
-        if (!wait_bounded(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+        if (!wait_inl<false>(&c->rempty, phr ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
         const uint32_t fr = mapa(saddr(&c->rfull), 0);
         if (rank == 0) mbar_expect_tx(&c->rfull, 4u * 32768u);
         const int qrow = p.c0 + 256 * qp + 128 * (int)rank;
@@ -655,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
         lph_r = phr;
         phr ^= 1u;
         for (int j = 0; j < nj; ++j) {
-          if (!wait_bounded(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          if (!wait_inl<false>(&c->aempty[sa], pha ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fa = mapa(saddr(&c->afull[sa]), 0);
           if (rank == 0) mbar_expect_tx(&c->afull[sa], 2u * Q_X_STAGE);
           const uint32_t st = sb + Q_X + sa * Q_X_STAGE;
@@ -673,9 +673,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
       if (!ok) {
         fail_f(c, p.status);
         if (rank == 0) {
-          if (iss & 4u) wait_bounded(&c->rfull, lph_r, nullptr, 200000000ull);
+          if (iss & 4u) wait_inl<false>(&c->rfull, lph_r, nullptr, 200000000ull);
           for (int s = 0; s < 2; ++s)
-            if (iss & (1u << s)) wait_bounded(&c->afull[s], lph_a[s], nullptr, 200000000ull);
+            if (iss & (1u << s)) wait_inl<false>(&c->afull[s], lph_a[s], nullptr, 200000000ull);
         }
       }
     } else if (lane == 16) {
@@ -688,7 +688,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
         int z, qp, nj;
         q_unit(p, u, z, qp, nj);
         for (int j = 0; j < nj; ++j) {
-          if (!wait_bounded(&c->bempty[sy], phy ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
+          if (!wait_inl<false>(&c->bempty[sy], phy ^ 1u, &c->abort, p.limit_ns)) { ok = false; break; }
           const uint32_t fb = mapa(saddr(&c->bfull[sy]), 0);
           if (rank == 0) mbar_expect_tx(&c->bfull[sy], 2u * Q_Y_STAGE);
           tma_load_3d_pair(sb + Q_Y + sy * Q_Y_STAGE, &tmKb, fb, 64 * (int)rank, 128 * j, z / p.group);
@@ -701,7 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
         fail_f(c, p.status);
         if (rank == 0)
           for (int s = 0; s < 2; ++s)
-            if (iss & (1u << s)) wait_bounded(&c->bfull[s], lph[s], nullptr, 200000000ull);
+            if (iss & (1u << s)) wait_inl<false>(&c->bfull[s], lph[s], nullptr, 200000000ull);
       }
     }
   } else if (warp == 1) {
@@ -714,7 +714,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
       // dQ += dS K for global key block gg (the first of its unit overwrites)
       auto accumulate = [&](uint32_t gg, bool first) -> bool {
         if (!wait_n(&c->oready, oready_seen, gg + 1, c, p.limit_ns)) return false;
-        if (!wait_bounded(&c->bfull[sy], phy, &c->abort, p.limit_ns)) return false;
+        if (!wait_inl<false>(&c->bfull[sy], phy, &c->abort, p.limit_ns)) return false;
         if (first && !wait_n(&c->accempty, acc_seen, (uint32_t)lu, c, p.limit_ns)) return false;
         tc_fence_after();
 #pragma unroll
@@ -730,12 +730,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
       for (int u = pid; u < p.n_units && ok; u += npairs, ++lu) {
         int z, qp, nj;
         q_unit(p, u, z, qp, nj);
-        if (!wait_bounded(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
+        if (!wait_inl<false>(&c->rfull, phr, &c->abort, p.limit_ns)) { ok = false; break; }
         phr ^= 1u;
         tc_fence_after();
         for (int n = 0; n < nj; ++n, ++g) {
           if (!wait_n(&c->tempty, tempty_seen, g, c, p.limit_ns)) { ok = false; break; }
-          if (!wait_bounded(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
+          if (!wait_inl<false>(&c->afull[sa], pha, &c->abort, p.limit_ns)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dst = dplus(dX, sa * Q_X_STAGE);
 #pragma unroll
@@ -757,7 +757,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
       }
       if (!ok) fail_f(c, p.status);
       commit2_mc(&c->mdone, 1);
-      wait_bounded(&c->mdone, 0, nullptr, 200000000ull);
+      wait_inl<false>(&c->mdone, 0, nullptr, 200000000ull);
     }
     __syncwarp();
   } else if (warp == Q_FWD_WARP) {

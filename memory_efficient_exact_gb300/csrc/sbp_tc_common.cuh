@@ -196,6 +196,23 @@ __device__ __forceinline__ bool wait_cluster(uint64_t* b, uint32_t parity, const
   if (try_cluster(b, parity)) return true;
   return wait_cluster_slow(b, parity, abort_flag, limit_ns);
 }
+// The same two waits with the spin loop inlined instead of called: no call-site register
+// saves (the fused attention kernels use these: k_attn_q then needs no local memory, and
+// the pair ran about 1% faster).  A register split between warpgroups (setmaxnreg) also
+// requires it, since a call would run under the kernel-wide register count.
+template <bool CLUSTER>
+__device__ __forceinline__ bool wait_inl(uint64_t* b, uint32_t parity, const volatile int* abort_flag,
+                                         uint64_t limit_ns) {
+  if (CLUSTER ? try_cluster(b, parity) : mbar_try(b, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (CLUSTER ? try_cluster(b, parity) : mbar_try(b, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (gtimer() - t0 > limit_ns) return false;
+    }
+  }
+}
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* b, uint32_t parity, Ctrl* c, uint64_t limit) {
   const bool ok = wait_cluster(b, parity, &c->abort, limit);
   return __all_sync(0xffffffffu, ok);
