@@ -19,7 +19,8 @@ The plain invocation also measures the other workloads -- GRPO, DPO, the two chu
 sweeps and the two sublayers, each in its own process after the main line's measurement --
 and folds their JSON lines under "other_workloads" (`--no-other-workloads` skips that).
 Other lines (each its own JSON line when run by itself):
-  --objective grpo|dpo          the other objectives (8 x 2048 / 8 x 4096 tokens)
+  --objective grpo|dpo [--chunk C]   the other objectives (8 x 2048 / 8 x 4096 tokens,
+                                chunk 2048 unless given)
   --workload sft_T8192_d2560|sft_T65536_d5120 [--chunk C]   the chunk-sweep workloads
   --workload profile            a small case of the same kernels for ncu captures
   --lean                        the one-buffer workspace schedule
@@ -232,8 +233,10 @@ def run_reference(args):
 # bench process after the main line (the plain invocation only); their JSON lines are
 # folded into the main line under "other_workloads", so that one run records them all.
 OTHER_WORKLOADS = [
-    ("grpo_8x2048_d4096_chunk4096", ["--objective", "grpo", "--steps", "10"]),
-    ("dpo_8x4096_d4096_chunk4096", ["--objective", "dpo", "--steps", "5"]),
+    ("grpo_8x2048_d4096_chunk2048", ["--objective", "grpo", "--steps", "10"]),
+    ("grpo_8x2048_d4096_chunk4096", ["--objective", "grpo", "--chunk", "4096", "--steps", "10"]),
+    ("dpo_8x4096_d4096_chunk2048", ["--objective", "dpo", "--steps", "5"]),
+    ("dpo_8x4096_d4096_chunk4096", ["--objective", "dpo", "--chunk", "4096", "--steps", "5"]),
     ("sft_T8192_d2560_chunk512", ["--workload", "sft_T8192_d2560", "--chunk", "512", "--steps", "10"]),
     ("sft_T8192_d2560_chunk1024", ["--workload", "sft_T8192_d2560", "--chunk", "1024", "--steps", "10"]),
     ("sft_T8192_d2560_chunk2048", ["--workload", "sft_T8192_d2560", "--chunk", "2048", "--steps", "10"]),
@@ -866,7 +869,8 @@ def main(argv=None):
     ap.add_argument("--sublayer", choices=["lmhead", "mlp", "attn"], default="lmhead",
                     help="mlp / attn: the chunked SwiGLU-MLP or causal-attention backward (own JSON line)")
     ap.add_argument("--objective", choices=["sft", "grpo", "dpo"], default="sft",
-                    help="grpo: 2048-token responses; dpo: 4096-token sequences, both passes per step")
+                    help="grpo: 8 responses of 2048 tokens; dpo: 8 sequences of 4096 tokens, both passes per "
+                         "step; chunk 2048 for both unless --chunk is given")
     args = ap.parse_args(argv)
     if args.workload == "profile":
         WORKLOAD.clear()
@@ -881,6 +885,8 @@ def main(argv=None):
     if args.objective == "dpo" and args.workload == "main":
         # the DPO input recipe: 8 sequences of 4096 tokens, the first 1024 of each masked
         WORKLOAD.update(T=32768, seed=1003, mask="seqhead", n=1024, seq_len=4096, frac=0.0)
+    if args.objective != "sft" and args.workload == "main":
+        WORKLOAD["chunk"] = 2048   # the GRPO and DPO workloads' own chunk
     for key, val in (("chunk", args.chunk), ("T", args.tokens), ("d", args.d)):
         if val is not None:
             WORKLOAD[key] = val

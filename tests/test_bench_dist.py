@@ -85,7 +85,11 @@ def test_other_workloads_ride_only_with_the_plain_invocation():
         assert _args_of(argv)["other"] is False, argv
     others = _args_of([])["others"]
     names = [n for n, _ in others]
-    assert len(set(names)) == len(names) and len(names) == 9
+    assert len(set(names)) == len(names) and len(names) == 11
+    # each folded line's name carries the chunk its command runs
+    for name, argv in others:
+        if name.startswith(("grpo", "dpo", "sft")):
+            assert name.endswith(f"_chunk{_args_of(argv)['chunk']}"), (name, argv)
 
 
 def test_bench_workload_selection():
@@ -99,9 +103,11 @@ def test_bench_workload_selection():
     assert w["workload"] == "sft_ce_lmhead_bf16_T8192_d2560_V151936_chunk512"
     w = _args_of(["--workload", "sft_T65536_d5120"])
     assert (w["T"], w["d"], w["chunk"], w["mask"], w["frac"]) == (65536, 5120, 4096, "frac", 0.05)
-    # DPO defaults to 8 sequences of 4096 tokens; GRPO keeps 8 x 2048
-    assert _args_of(["--objective", "dpo"])["T"] == 32768
-    assert _args_of(["--objective", "grpo"])["T"] == 16384
+    # DPO defaults to 8 sequences of 4096 tokens, GRPO to 8 x 2048, both at chunk 2048
+    assert (_args_of(["--objective", "dpo"])["T"], _args_of(["--objective", "dpo"])["chunk"]) == (32768, 2048)
+    assert (_args_of(["--objective", "grpo"])["T"], _args_of(["--objective", "grpo"])["chunk"]) == (16384, 2048)
+    w = _args_of(["--objective", "grpo", "--chunk", "4096"])
+    assert w["chunk"] == 4096 and w["workload"] == "grpo_clip_lmhead_bf16_T16384_d4096_V151936_chunk4096"
     # the profile case for ncu captures
     w = _args_of(["--workload", "profile"])
     assert (w["T"], w["V"], w["chunk"]) == (8192, 32768, 4096)
