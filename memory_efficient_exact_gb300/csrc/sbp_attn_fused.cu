@@ -36,7 +36,11 @@ namespace fa {
 // barriers; the forwarder turns each completed local phase into one arrival at the
 // leader, which keeps the remote arrival's latency off the epilogue's critical path.
 constexpr int FA_EPI = 16;
-constexpr int KV_LD_WARP = 2 + FA_EPI, KV_FWD_WARP = KV_LD_WARP + 1, Q_FWD_WARP = 2 + FA_EPI;
+// k_attn_kv: eight epilogue warps of 64 columns each (12 warps in all, so 168 registers a
+// thread): its epilogue measured 1490 cycles per block this way against 2350 for sixteen
+// warps of 32 columns held to 96 registers, the same work spilling.
+constexpr int KV_EPI = 8;
+constexpr int KV_LD_WARP = 2 + KV_EPI, KV_FWD_WARP = KV_LD_WARP + 1, Q_FWD_WARP = 2 + FA_EPI;
 constexpr int KV_THREADS = 32 * (KV_FWD_WARP + 1);
 constexpr int Q_THREADS = 32 * (Q_FWD_WARP + 1);
 constexpr uint32_t IDESC_KK = idesc_bf16(256, 128, false, false);  // A, B K-major
@@ -86,7 +90,7 @@ constexpr size_t SMEM_KV = KV_CTRL + sizeof(CtrlF) + 1024;
 constexpr size_t SMEM_Q = Q_CTRL + sizeof(CtrlF) + 1024;
 static_assert(SMEM_KV <= 232448, "k_attn_kv shared memory");
 
-__device__ __forceinline__ void prologue_f(CtrlF* c, int warp) {
+__device__ __forceinline__ void prologue_f(CtrlF* c, int warp, int epi) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->afull[i], 1);
@@ -99,15 +103,15 @@ __device__ __forceinline__ void prologue_f(CtrlF* c, int warp) {
     mbar_init(&c->tfull, 1);
     mbar_init(&c->tempty, 2);
     mbar_init(&c->oready, 2);
-    mbar_init(&c->tempty_l, FA_EPI);
-    mbar_init(&c->oready_l, FA_EPI);
+    mbar_init(&c->tempty_l, epi);
+    mbar_init(&c->oready_l, epi);
     mbar_init(&c->ofree, 1);
     mbar_init(&c->dsfree[0], 1);
     mbar_init(&c->dsfree[1], 1);
-    mbar_init(&c->accempty, 2 * FA_EPI);
+    mbar_init(&c->accempty, 2 * epi);
     mbar_init(&c->lfull, 1);
-    mbar_init(&c->lempty, FA_EPI);
-    mbar_init(&c->sfree, FA_EPI);
+    mbar_init(&c->lempty, epi);
+    mbar_init(&c->sfree, epi);
     mbar_init(&c->mdone, 1);
     c->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -233,6 +237,43 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 // ================================================================ k_attn_kv (dK, dV)
 
+// One round of k_attn_kv's epilogue: 16 queries (columns j0 .. j0+15 of the thread's
+// 32-column group) of this thread's key row.  P^T = 2^(s S^T - lse log2 e) and
+// dS^T = P^T (dP^T - D), packed to bf16 pairs.  MASK: the round holds queries before the
+// key or past the chunk's end (a diagonal block or the ragged tail), which get P = 0; the
+// other rounds skip the per-element test (the mask costs more than the math it guards).
+template <bool MASK>
+__device__ __forceinline__ void kv_round(const uint32_t (&rs)[32], const uint32_t (&rd)[32], int j0,
+                                         const float* lds, float sl2, int qg, int key, int c1, uint32_t* pw,
+                                         uint32_t* dw) {
+  const float4* l4 = reinterpret_cast<const float4*>(lds);
+  const float4* d4 = reinterpret_cast<const float4*>(lds + 128);
+#pragma unroll
+  for (int j4 = 0; j4 < 4; ++j4) {
+    const float4 L = l4[j4], Dv = d4[j4];
+    const float lz[4] = {L.x, L.y, L.z, L.w}, dz[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+    float pv[4], sv[4];
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      const int j = j0 + 4 * j4 + e;
+      const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[j]), sl2, -lz[e]),
+                                  fmaf(__uint_as_float(rs[j + 1]), sl2, -lz[e + 1]));
+      pv[e] = pp.x;
+      pv[e + 1] = pp.y;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = 4 * j4 + e;
+      if (MASK && (qg + j < key || qg + j >= c1)) pv[e] = 0.f;
+      sv[e] = pv[e] * (__uint_as_float(rd[j0 + j]) - dz[e]);
+    }
+    pw[2 * j4] = pack_bf16(pv[0], pv[1]);
+    pw[2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
+    dw[2 * j4] = pack_bf16(sv[0], sv[1]);
+    dw[2 * j4 + 1] = pack_bf16(sv[2], sv[3]);
+  }
+}
+
 struct KvP {
   int H, T, c0, c1, nb, n_units;
   int Hkv, group;    // key / value heads; query heads per key / value head (H = Hkv * group)
@@ -273,7 +314,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
   const uint32_t sb = saddr(base);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
-  prologue_f(c, warp);
+  prologue_f(c, warp, KV_EPI);
   const uint32_t tmem = c->tmem_base;
   const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
@@ -467,7 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
       }
     }
   } else {
-    const int q = warp & 3, cg = (warp - 2) >> 2;   // lane quadrant, 32-column group
+    const int q = warp & 3, ch = (warp - 2) >> 2;   // lane quadrant; 64-column half of the block
     const int lrow = q * 32 + lane;
     const uint32_t trow = (uint32_t)(q * 32) << 16;
     const float sl2 = p.scale * L2E;
@@ -487,50 +528,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         if (!warp_wait_n(&c->tfull, tfull_seen, g + 1, c, p.limit_ns) ||
             !warp_wait_n(&c->lfull, lfull_seen, g + 1, c, p.limit_ns)) { ok = false; break; }
         tc_fence_after();
-        uint32_t pw[16], dw[16];   // bf16 pairs of P^T and dS^T over this thread's 32 queries
-        uint32_t rs[32], rd[32];
-        tmem_ld32(tmem + trow + (uint32_t)(32 * cg), rs);
-        tmem_ld32(tmem + trow + (uint32_t)(128 + 32 * cg), rd);
-        tmem_ld_wait();
-        // S^T and dP^T are in registers: the next block's may be formed
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c->tempty_l);
+        uint32_t pw[2][16], dw[2][16];   // bf16 pairs of P^T and dS^T over this thread's 64 queries
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {   // two rounds of 16 queries
-          const int qg = p.c0 + 128 * b + 32 * cg + 16 * r;   // first query of the round
-          const bool none = qg + 15 < kw || qg >= p.c1;
-          const bool all = qg >= kw + 31 && qg + 15 < p.c1;
-          if (none) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) pw[8 * r + j] = dw[8 * r + j] = 0u;
-            continue;
+        for (int h = 0; h < 2; ++h) {   // the half's two 32-column groups, one after the other
+          const int cg = 2 * ch + h;
+          uint32_t rs[32], rd[32];
+          tmem_ld32(tmem + trow + (uint32_t)(32 * cg), rs);
+          tmem_ld32(tmem + trow + (uint32_t)(128 + 32 * cg), rd);
+          tmem_ld_wait();
+          if (h == 1) {   // S^T and dP^T are all in registers: the next block's may be formed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c->tempty_l);
           }
-          const float4* l4 = reinterpret_cast<const float4*>(ld + 32 * cg + 16 * r);
-          const float4* d4 = reinterpret_cast<const float4*>(ld + 128 + 32 * cg + 16 * r);
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const float4 L = l4[j4], Dv = d4[j4];
-            const float lz[4] = {L.x, L.y, L.z, L.w}, dz[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
-            float pv[4], sv[4];
+          for (int r = 0; r < 2; ++r) {   // two rounds of 16 queries
+            const int qg = p.c0 + 128 * b + 32 * cg + 16 * r;   // first query of the round
+            const bool none = qg + 15 < kw || qg >= p.c1;
+            const bool all = qg >= kw + 31 && qg + 15 < p.c1;
+            if (none) {
 #pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-              const int j = 16 * r + 4 * j4 + e;
-              const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[j]), sl2, -lz[e]),
-                                          fmaf(__uint_as_float(rs[j + 1]), sl2, -lz[e + 1]));
-              pv[e] = pp.x;
-              pv[e + 1] = pp.y;
+              for (int j = 0; j < 8; ++j) pw[h][8 * r + j] = dw[h][8 * r + j] = 0u;
+            } else if (all) {
+              kv_round<false>(rs, rd, 16 * r, ld + 32 * cg + 16 * r, sl2, qg, key, p.c1, &pw[h][8 * r], &dw[h][8 * r]);
+            } else {
+              kv_round<true>(rs, rd, 16 * r, ld + 32 * cg + 16 * r, sl2, qg, key, p.c1, &pw[h][8 * r], &dw[h][8 * r]);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 4 * j4 + e;
-              if (!all && (qg + j < key || qg + j >= p.c1)) pv[e] = 0.f;
-              sv[e] = pv[e] * (__uint_as_float(rd[16 * r + j]) - dz[e]);
-            }
-            pw[8 * r + 2 * j4] = pack_bf16(pv[0], pv[1]);
-            pw[8 * r + 2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
-            dw[8 * r + 2 * j4] = pack_bf16(sv[0], sv[1]);
-            dw[8 * r + 2 * j4 + 1] = pack_bf16(sv[2], sv[3]);
           }
         }
         __syncwarp();
@@ -539,23 +562,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
         // block, also the previous unit's dV / dK staging has left this area
         if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns) ||
             (n == 0 && !warp_wait_n(&c->sfree, sfree_seen, (uint32_t)lu, c, p.limit_ns))) { ok = false; break; }
-        store_half_row(sb + KV_PT + (cg >> 1) * 16384, lrow, cg & 1, pw);
-        store_half_row(sb + KV_DST + (cg >> 1) * 16384, lrow, cg & 1, dw);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          store_half_row(sb + KV_PT + ch * 16384, lrow, h, pw[h]);
+          store_half_row(sb + KV_DST + ch * 16384, lrow, h, dw[h]);
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&c->oready_l);
       }
       if (!ok) break;
-      // the unit's dV and dK: out of tensor memory, through this warp's 4 KB of the
-      // P^T / dS^T area, added into the fp32 outputs.  Each output element receives one
-      // add per launch; rows past T are clipped by the tensor map, rows in [c1, T) add 0.
+      // the unit's dV and dK: out of tensor memory, through this warp's 8 KB of the
+      // P^T / dS^T area (one 4 KB block per 32 columns), added into the fp32 outputs.
+      // Each output element receives one add per launch; rows past T are clipped by the
+      // tensor map, rows in [c1, T) add 0.
       if (!warp_wait_n(&c->ofree, ofree_seen, g, c, p.limit_ns)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t stg = sb + KV_PT + (uint32_t)(warp - 2) * 4096u;
+      const uint32_t stg = sb + KV_PT + (uint32_t)(warp - 2) * 8192u;
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {   // t = 0: dV, t = 1: s dK
-        uint32_t ra[32];
-        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 32 * cg), ra);
+        uint32_t ra[2][32];
+        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 64 * ch), ra[0]);
+        tmem_ld32(tmem + trow + (uint32_t)((t ? 384 : 256) + 64 * ch + 32), ra[1]);
         tmem_ld_wait();
         if (t == 1) {   // both accumulators are in registers: the next unit may overwrite them
           tc_fence_before();
@@ -568,16 +596,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
           __syncwarp();
         }
         const float f = t ? p.scale : 1.f;
-        const uint32_t buf = stg + (uint32_t)lane * 128u;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          sts128(buf + ((uint32_t)(k ^ (lane & 7)) << 4), __float_as_uint(__uint_as_float(ra[4 * k]) * f),
-                 __float_as_uint(__uint_as_float(ra[4 * k + 1]) * f), __float_as_uint(__uint_as_float(ra[4 * k + 2]) * f),
-                 __float_as_uint(__uint_as_float(ra[4 * k + 3]) * f));
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t buf = stg + (uint32_t)h * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            sts128(buf + ((uint32_t)(k ^ (lane & 7)) << 4), __float_as_uint(__uint_as_float(ra[h][4 * k]) * f),
+                   __float_as_uint(__uint_as_float(ra[h][4 * k + 1]) * f),
+                   __float_as_uint(__uint_as_float(ra[h][4 * k + 2]) * f),
+                   __float_as_uint(__uint_as_float(ra[h][4 * k + 3]) * f));
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_3d(t ? &tmdK : &tmdV, stg, 32 * cg, kw, zk);
+          tma_reduce_add_3d(t ? &tmdK : &tmdV, stg, 64 * ch, kw, zk);
+          tma_reduce_add_3d(t ? &tmdK : &tmdV, stg + 4096u, 64 * ch + 32, kw, zk);
           bulk_commit();
         }
       }
@@ -593,6 +626,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(KV_THREADS, 1)
 }
 
 // ===================================================================== k_attn_q (dQ)
+
+// One round of k_attn_q's epilogue: 16 keys of this thread's query row.  P = 2^(s S -
+// lse log2 e), dS = P (dP - D), packed to bf16 pairs.  MASK: the round holds keys after
+// the query (the diagonal block) or the row is past the chunk's end; the other rounds
+// skip the per-element test.
+template <bool MASK>
+__device__ __forceinline__ void q_round(const uint32_t (&rs)[16], const uint32_t (&rd)[16], float sl2, float lz,
+                                        float Dq, int kg, int qr, bool vrow, uint32_t* dw) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[2 * i]), sl2, -lz),
+                                fmaf(__uint_as_float(rs[2 * i + 1]), sl2, -lz));
+    float pv[2] = {pp.x, pp.y}, sv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int jj = 2 * i + e;
+      if (MASK && (kg + jj > qr || !vrow)) pv[e] = 0.f;
+      sv[e] = pv[e] * (__uint_as_float(rd[jj]) - Dq);
+    }
+    dw[i] = pack_bf16(sv[0], sv[1]);
+  }
+}
 
 struct QP {
   int H, T, c0, c1, n_qp, n_units;
@@ -625,7 +680,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
   const uint32_t sb = saddr(base);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
-  prologue_f(c, warp);
+  prologue_f(c, warp, FA_EPI);
   const uint32_t tmem = c->tmem_base;
   const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
@@ -810,20 +865,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
           if (none) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) dw[8 * r + i] = 0u;
-            continue;
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 pp = exp2_pair(fmaf(__uint_as_float(rs[2 * i]), sl2, -lz),
-                                        fmaf(__uint_as_float(rs[2 * i + 1]), sl2, -lz));
-            float pv[2] = {pp.x, pp.y}, sv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int jj = 2 * i + e;
-              if (!all && (kg + jj > qr || !vrow)) pv[e] = 0.f;
-              sv[e] = pv[e] * (__uint_as_float(rd[jj]) - Dq);
-            }
-            dw[8 * r + i] = pack_bf16(sv[0], sv[1]);
+          } else if (all) {
+            q_round<false>(rs, rd, sl2, lz, Dq, kg, qr, vrow, &dw[8 * r]);
+          } else {
+            q_round<true>(rs, rd, sl2, lz, Dq, kg, qr, vrow, &dw[8 * r]);
           }
         }
         // dS into tensor-memory buffer g % 2 once the dQ GEMM of its previous block has read it
