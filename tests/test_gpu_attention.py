@@ -4,8 +4,9 @@ Inputs: Q, K, V, dO ~ N(0, 1) rounded to bf16; O and lse from the oracle's forwa
 same values (O rounded to bf16, lse kept in fp32, as a forward saves them); the expected
 gradients are the oracle's unchunked backward on exactly the values the GPU sees.
 Shapes span several heads, several chunks with a ragged last one, row pairs and 256-key
-tiles; dQ / dK / dV relative Frobenius error <= 2e-2 (the bf16 tolerance of the other
-tests).
+tiles; the benchmark's size (T=8192) and the long-sequence one (T=32768, grouped heads) on
+sampled rows and keys; dQ / dK / dV relative Frobenius error <= 2e-2 (the bf16 tolerance
+of the other tests).
 """
 import numpy as np
 import pytest
@@ -209,3 +210,56 @@ def test_side_stream_under_graph_capture_and_threads(sbp):
         sbp.check_status(o["status"])
         for k in ("dQ", "dK", "dV"):
             assert torch.equal(o[k], ref[k]), k
+
+
+def test_attention_long_T32768_gqa_sampled(sbp):
+    """The long-sequence workload of the attention measurements: T=32768, 32 query heads on
+    8 key / value heads, hd=128, at chunks 4096 and 8192.  O and lse come from a plain fp32
+    torch forward on the device (O rounded to bf16, as a forward saves it); the oracle's
+    row and column forms take exactly those values, so the check is of the backward alone:
+    dQ on sampled query rows of the first and last query heads, dK / dV on sampled keys of
+    the first and last key / value heads (chunk edges, the first and last token, random
+    picks), each against the float64 oracle."""
+    H, Hkv, T, hd = 32, 8, 32768, 128
+    grp = H // Hkv
+    g = np.random.default_rng(327680)
+    Q, dO = (I.round_bf16(g.standard_normal((H, T, hd), dtype=np.float32)) for _ in range(2))
+    K, V = (I.round_bf16(g.standard_normal((Hkv, T, hd), dtype=np.float32)) for _ in range(2))
+    scale = 1.0 / np.sqrt(hd)
+    tq, tk, tv, tdo = dev(Q), dev(K), dev(V), dev(dO)
+    O = torch.empty_like(tq)
+    lse = torch.empty((H, T), dtype=torch.float32, device="cuda")
+    mask = torch.ones((T, T), dtype=torch.bool, device="cuda").triu(1)
+    for h in range(H):
+        S = (tq[h].float() @ tk[h // grp].float().T) * scale
+        S.masked_fill_(mask, float("-inf"))
+        lse[h] = torch.logsumexp(S, dim=1)
+        S.sub_(lse[h][:, None]).exp_()
+        O[h] = (S @ tv[h // grp].float()).to(torch.bfloat16)
+    del S, mask
+    torch.cuda.empty_cache()
+    On = O.float().cpu().numpy()
+    lsen = lse.cpu().numpy()
+    edges = [0, 1, 127, 128, 4095, 4096, 8191, 8192, 16383, 16384, 24576, 32766, 32767]
+    rows = sorted(set(edges) | set(g.integers(0, T, 16).tolist()))
+    keys = sorted(set(edges) | set(g.integers(0, T, 16).tolist()))
+    # the oracle on the heads it checks only (each call takes one query head, or one key /
+    # value head with its group)
+    rq = {h: A.rows_dQ(Q[h:h + 1], K[h // grp:h // grp + 1], V[h // grp:h // grp + 1], On[h:h + 1],
+                       dO[h:h + 1], lsen[h:h + 1], scale, 0, rows) for h in (0, H - 1)}
+    rkv = {}
+    for hk in (0, Hkv - 1):
+        qs = slice(hk * grp, (hk + 1) * grp)
+        rkv[hk] = A.keys_dKdV(Q[qs], K[hk:hk + 1], V[hk:hk + 1], On[qs], dO[qs], lsen[qs], scale, 0, keys)
+    for chunk in (4096, 8192):
+        out = sbp.attn_causal_backward(tq, tk, tv, O, tdo, lse, scale, chunk)
+        torch.cuda.synchronize()
+        sbp.check_status(out["status"])
+        dQ = out["dQ"].float().cpu().numpy()
+        dK, dV = out["dK"].cpu().numpy(), out["dV"].cpu().numpy()
+        del out
+        for h, r in rq.items():
+            assert rel_fro(dQ[h][rows], r) <= 2e-2, (chunk, h, rel_fro(dQ[h][rows], r))
+        for hk, (rk, rv) in rkv.items():
+            e = {"dK": rel_fro(dK[hk][keys], rk), "dV": rel_fro(dV[hk][keys], rv)}
+            assert max(e.values()) <= 2e-2, (chunk, hk, e)
