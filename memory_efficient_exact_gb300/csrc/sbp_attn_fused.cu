@@ -29,18 +29,19 @@ namespace sbp {
 namespace tc {
 namespace fa {
 
-// Warps: 0 TMA producers, 1 MMA issuer, 2-17 epilogue (lane quadrant warp % 4, 32 of the
-// 128 columns each: sixteen warps, so that the exp / scale / pack chains of four warps
-// per scheduler hide each other's latency), then (k_attn_kv) one warp that stages lse
-// and D per block, and one forwarder warp.  The epilogue warps arrive on CTA-local
-// barriers; the forwarder turns each completed local phase into one arrival at the
-// leader, which keeps the remote arrival's latency off the epilogue's critical path.
-constexpr int FA_EPI = 16;
+// Warps: 0 TMA producers, 1 MMA issuer, then the epilogue warps (lane quadrant warp % 4),
+// then (k_attn_kv) one warp that stages lse and D per block, and one forwarder warp.  The
+// epilogue warps arrive on CTA-local barriers; the forwarder turns each completed local
+// phase into one arrival at the leader, which keeps the remote arrival's latency off the
+// epilogue's critical path.
+// k_attn_q: sixteen epilogue warps of 32 of the 128 columns each (19 warps, 85 registers
+// a thread, no spills; eight warps of 64 columns measured the same).
+constexpr int Q_EPI = 16;
 // k_attn_kv: eight epilogue warps of 64 columns each (12 warps in all, so 168 registers a
 // thread): its epilogue measured 1490 cycles per block this way against 2350 for sixteen
 // warps of 32 columns held to 96 registers, the same work spilling.
 constexpr int KV_EPI = 8;
-constexpr int KV_LD_WARP = 2 + KV_EPI, KV_FWD_WARP = KV_LD_WARP + 1, Q_FWD_WARP = 2 + FA_EPI;
+constexpr int KV_LD_WARP = 2 + KV_EPI, KV_FWD_WARP = KV_LD_WARP + 1, Q_FWD_WARP = 2 + Q_EPI;
 constexpr int KV_THREADS = 32 * (KV_FWD_WARP + 1);
 constexpr int Q_THREADS = 32 * (Q_FWD_WARP + 1);
 constexpr uint32_t IDESC_KK = idesc_bf16(256, 128, false, false);  // A, B K-major
@@ -680,7 +681,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Q_THREADS, 1)
   const uint32_t sb = saddr(base);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ctarank();
-  prologue_f(c, warp, FA_EPI);
+  prologue_f(c, warp, Q_EPI);
   const uint32_t tmem = c->tmem_base;
   const int pid = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
