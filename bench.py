@@ -63,10 +63,11 @@ SWEEP_WORKLOADS = {
 }
 CPU_SAMPLE_TOKENS = 384
 # DRAM bytes (read + write) of one accumulating k_bwd launch, from an ncu capture of the
-# profile workload (d = 4096, chunk 4096, V = 32768: 2.450 GB read + 0.567 GB written),
+# profile workload (d = 4096, chunk 4096, V = 32768: 2.160 GB read + 0.565 GB written),
 # scaled to V = 151936 by the units processed (every operand but H_c grows with V).  Only
-# valid for the main workload's shape and the kernel version it was captured on.
-K_BWD_TRAFFIC_BYTES = (2.450e9 + 0.567e9) * 151936 / 32768
+# valid for the main workload's shape and the kernel version it was captured on (dH units
+# in bands of 8 row tiles).
+K_BWD_TRAFFIC_BYTES = (2.160e9 + 0.565e9) * 151936 / 32768
 
 
 def load_peaks():

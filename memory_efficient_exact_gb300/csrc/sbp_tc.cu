@@ -351,15 +351,31 @@ struct Unit {
   int z;   // problem of the batch
 };
 
+// dH units of one split run in bands of kDhBand row tiles: a band's units cover its row
+// tiles for every column tile of d, row tiles fastest.  A wave of 76 SM pairs then holds
+// about 8 row tiles x 9.5 column tiles, so G's k-blocks (one per row tile) and W's (one per
+// column tile) are each fetched about twice per wave, instead of G about 3.4 times and W
+// once when all 16 row tiles of a 4096-row chunk come first.  Measured on the profile case
+// (chunk 4096, d 4096, V 32768): 5.4% less DRAM traffic per k_bwd launch and 1.5% more
+// tokens per MHz on the bench workload.  Only the order changes: the partials of each
+// split are summed in a fixed order, so the results are the same bits.
+constexpr int kDhBand = 8;
+
 __device__ __forceinline__ Unit decode(const BwdP& p, int u) {
   Unit w;
   if (u < p.n_dh) {
     w.kind = 0;
     w.z = u / p.n_dh_b;
     u -= w.z * p.n_dh_b;
-    w.mp = u % p.mt_c;
-    w.nb = (u / p.mt_c) % p.nt_d;
-    w.split = u / (p.mt_c * p.nt_d);
+    const int per = p.mt_c * p.nt_d;
+    w.split = u / per;
+    const int t = u - w.split * per;
+    const int R = p.mt_c < kDhBand ? p.mt_c : kDhBand;
+    const int band = t / (R * p.nt_d);
+    const int t2 = t - band * R * p.nt_d;
+    const int rk = p.mt_c - band * R < R ? p.mt_c - band * R : R;   // row tiles in this band
+    w.mp = band * R + t2 % rk;
+    w.nb = t2 / rk;
     w.kb0 = (int)((int64_t)w.split * p.kb_v / p.splits);
     w.kb1 = (int)((int64_t)(w.split + 1) * p.kb_v / p.splits);
   } else {
