@@ -633,6 +633,15 @@ ATTN_WORKLOAD = dict(H=32, T=8192, hd=128, chunk=4096, seed=1006)
 ATTN_METRIC = "attention bwd tokens/s (causal, H=32, hd=128, T=8192)"
 
 
+def attn_pairs(T: int, chunk: int):
+    """(causal, rectangles): the (query, key) pairs of one head that the method's GEMMs
+    cover, q >= k, T (T + 1) / 2 of them whatever the chunk; and the pairs of the chunk
+    rectangles (each chunk's queries x every key up to the chunk's end, the diagonal
+    blocks' masked half included), what the chunk-buffer path computes and stores."""
+    rect = sum(min(chunk, T - c0) * min(T, c0 + chunk) for c0 in range(0, T, chunk))
+    return T * (T + 1) // 2, rect
+
+
 def attn_forward_inputs(torch, Q, K, V, scale):
     """O and the row log-sum-exp of the causal forward, head by head in fp32 (input set-up
     with plain torch ops, outside the timed region); K, V may have H / group heads."""
@@ -707,11 +716,8 @@ def run_attn_bench(args):
     value = T * args.steps / (ms / 1000.0)
     peaks, src = load_peaks()
     # algorithmic FLOPs: five GEMMs (S, dP, dQ, dK, dV) of 2 hd per causal (query, key)
-    # pair, q >= k: T (T + 1) / 2 pairs per head, whatever the chunk.  The chunk
-    # rectangles (a chunk's queries x every key up to its end, the diagonal block's masked
-    # half included) are what the chunk-buffer path computes and stores
-    rowkeys = sum(min(chunk, T - c0) * min(T, c0 + chunk) for c0 in range(0, T, chunk))
-    causal = T * (T + 1) // 2
+    # pair; the chunk rectangles are what the chunk-buffer path computes and stores
+    causal, rowkeys = attn_pairs(T, chunk)
     flops = 5 * 2 * hd * H * causal
     fused = hd == 128   # P and dS stay on chip (k_attn_kv, k_attn_q); else chunk buffers in HBM
     # chunk buffers: P and dS written once and read twice each (2 bytes an element)

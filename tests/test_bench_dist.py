@@ -112,3 +112,23 @@ def test_bench_workload_selection():
     w = _args_of(["--workload", "profile"])
     assert (w["T"], w["V"], w["chunk"]) == (8192, 32768, 4096)
     assert _args_of(["--sublayer", "attn"])["sublayer"] == "attn"
+
+
+def test_attention_pair_counts():
+    """The attention line's FLOP accounting: causal pairs T (T + 1) / 2 whatever the chunk;
+    chunk rectangles (n + 1) / n times that, n = T / chunk, when the chunk divides T (the
+    chunks' sum of c (i + 1) c over i < n), and equal to the full square for one chunk."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_pairs_probe", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    for T, chunk in ((8192, 1024), (8192, 4096), (4096, 4096), (32768, 4096)):
+        causal, rect = b.attn_pairs(T, chunk)
+        n = T // chunk
+        assert causal == T * (T + 1) // 2
+        assert rect == chunk * chunk * n * (n + 1) // 2
+    assert b.attn_pairs(8192, 8192)[1] == 8192 * 8192
+    # a ragged last chunk: chunks of 3 over T = 7 -> rows 3, 3, 1 reading keys 3, 6, 7
+    assert b.attn_pairs(7, 3) == (28, 3 * 3 + 3 * 6 + 1 * 7)
+    # brute force on a small case: the causal pairs q >= k, counted one by one
+    assert b.attn_pairs(37, 5)[0] == sum(1 for q in range(37) for k in range(q + 1))
