@@ -157,6 +157,43 @@ def test_dpo_parity(sbp, dtype, lens, d, V, chunk):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_dpo_saturated_margins(sbp, dtype):
+    """DPO with the sigmoid far in both tails: the references are set so that the pairs'
+    margins are about +5000, -500, +30 and 0 (beta = 0.5).  sigma(-m) underflows to 0 for
+    the first, is 1 to fp64 precision for the second; the loss is log(1 + e^-m) summed
+    stably (about 500 + 2e-13 + log 2 here, mean over pairs) and the gradient scales
+    -beta sigma(-m) must stay finite.  Loss, margins and full dH / dW against the oracle."""
+    lens = [60, 50, 40, 30, 60, 50, 40, 30]   # pairs (0, 4), (1, 5), (2, 6), (3, 7)
+    d, V, chunk = 64, 704, 64   # V a multiple of 8 (bf16 rows of W 16-byte aligned)
+    T = sum(lens)
+    H, W = I.make_hw(T, d, V, 4242, dtype, w_std=0.1)
+    y = I.make_labels(T, V, 4242, "frac", 0.1)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    beta = 0.5
+    f = O.dpo_pass1(H, W, y, cu, IGN)
+    x = np.array([1e4, -1e3, 60.0, 0.0])          # margins beta * x
+    ref_S = f["seq_logp"].copy()
+    ref_S[:4] -= x                                 # chosen: S_c - ref_c = x, rejected: 0
+    Ht, Wt, yt = to_dev(torch, H, W, y, dtype)
+    cut = torch.from_numpy(cu).cuda()
+    p1 = sbp.dpo_pass1(Ht, Wt, yt, cut, chunk)
+    p2 = sbp.dpo_pass2(Ht, Wt, yt, cut, p1["seq_logp"], torch.from_numpy(ref_S).cuda(), beta, chunk)
+    torch.cuda.synchronize()
+    sbp.check_status(p1["status"])
+    sbp.check_status(p2["status"])
+    tol = TOL[dtype]
+    ref = O.dpo(H, W, y, cu, ref_S, beta, IGN)
+    m = p2["margins"].cpu().numpy()
+    assert np.all(np.isfinite(m)) and np.isfinite(p2["loss"].item())
+    np.testing.assert_allclose(m, ref["margins"], rtol=0, atol=50 * tol["seq"] * np.abs(f["seq_logp"]).max())
+    assert m[0] > 4000 and m[1] < -400 and abs(m[3]) < 1
+    assert rel(p2["loss"].item(), ref["loss"]) <= tol["loss"]
+    dH, dW = p2["dH"].float().cpu().numpy(), p2["dW"].cpu().numpy()
+    assert np.all(np.isfinite(dH)) and np.all(np.isfinite(dW))
+    check_grads(dtype, p2, ref, y)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_accumulate_dw_and_determinism(sbp, dtype):
     T, d, V, chunk = 200, 128, 1000, 64
     H, W, y = make_case(T, d, V, dtype, seed=5, w_std=0.1)
